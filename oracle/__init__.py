@@ -1,0 +1,201 @@
+"""Float64 CPU oracle for the fused exact-attention forward pass.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The product path (the
+CUDA library and its Python binding) never imports, links or runs it, and it
+shares no code with them; the two meet only through the seeded input
+generators, which hold none of the method's arithmetic.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, float64, OpenMP over rows);
+this module builds it with gcc and marshals numpy arrays into it.
+
+Pages cited (titles as published):
+  [WGC] "Warp Group Cluster 优化：Flash Attention V3 在 H100 上的 FP8 融合计算实践"
+  [JJ]  "大模型加速-核心网络算子-Flash Attention V3"
+  [YT]  "FlashAttention V3：优化框架吞吐量的关键技术实践"
+
+Functions and the passage each follows:
+  attn_f64 / attn_rows_f64   standard attention, the exact result the method
+                             reaches ([WGC] §背景; [YT] §1.2 fused softmax+mask+matmul)
+  online_replay_f64          block-wise online softmax ([WGC] §2 GEMM-Softmax 融合流水线)
+  key_allowed                mask sets ([YT] §2.1.2 稀疏性感知的Mask优化)
+  e4m3_encode / e4m3_decode  E4M3 format ([JJ] §1.5 低精度FP8)
+  quantize_fp8_blockwise     per-block scaling ([WGC] §3 FP8 量化与精度保持)
+  dequantize                 x ~= x8 * scale for the block, the inverse map
+Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+E4M3_MAX = 448.0
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` into ``oracle/_build/liboracle.so`` with gcc."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        fp = ctypes.POINTER(ctypes.c_float)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lp = ctypes.POINTER(ctypes.c_long)
+        L, I, D = ctypes.c_long, ctypes.c_int, ctypes.c_double
+        lib.oracle_key_allowed.argtypes = [L, L, L, I, L]
+        lib.oracle_key_allowed.restype = I
+        lib.oracle_attn_rows_f64.argtypes = [dp, dp, dp, L, L, D, I, L, lp, L, dp, dp, I]
+        lib.oracle_attn_rows_f64.restype = I
+        lib.oracle_attn_f64.argtypes = [dp, dp, dp, L, L, L, D, I, L, dp, dp, I]
+        lib.oracle_attn_f64.restype = I
+        lib.oracle_online_replay_f64.argtypes = [dp, dp, dp, L, L, D, I, L, L, L, D, dp, dp]
+        lib.oracle_online_replay_f64.restype = None
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_float
+        lib.oracle_e4m3_encode_array.argtypes = [fp, u8p, L]
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_quantize_fp8_blockwise.argtypes = [fp, u8p, fp, L, L, L, L]
+        lib.oracle_quantize_fp8_blockwise.restype = None
+        _lib = lib
+        return lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to contiguous float64 (bf16 and fp32 values are representable)."""
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu")
+        import torch
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def key_allowed(i: int, j: int, N: int, causal: bool, window: int) -> bool:
+    return bool(_load().oracle_key_allowed(i, j, N, int(causal), int(window)))
+
+
+def attn_f64(q, k, v, scale: float, causal: bool = False, window: int = 0,
+             nthreads: int = 0):
+    """All rows of every head.  q, k, v: [..., N, d] -> (O [..., N, d], LSE [..., N])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    shape = q.shape
+    N, d = shape[-2], shape[-1]
+    BH = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    o = np.empty(shape, dtype=np.float64)
+    lse = np.empty(shape[:-1], dtype=np.float64)
+    _load().oracle_attn_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                            _ptr(v, ctypes.c_double), BH, N, d, float(scale), int(causal),
+                            int(window), _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                            int(nthreads))
+    return o, lse
+
+
+def attn_rows_f64(q, k, v, rows, scale: float, causal: bool = False, window: int = 0,
+                  nthreads: int = 0, return_threads: bool = False):
+    """Selected query rows of ONE head.  q, k, v: [N, d]; rows: R indices.
+
+    Returns (O [R, d], LSE [R]) (and the thread count when ``return_threads``).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= N):
+        raise ValueError("row index out of range")
+    R = rows.size
+    o = np.empty((R, d), dtype=np.float64)
+    lse = np.empty((R,), dtype=np.float64)
+    nt = _load().oracle_attn_rows_f64(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double), N, d,
+        float(scale), int(causal), int(window), _ptr(rows, ctypes.c_long), R,
+        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(nthreads))
+    if return_threads:
+        return o, lse, nt
+    return o, lse
+
+
+def online_replay_f64(q, k, v, scale: float, causal: bool, window: int, BM: int, BN: int,
+                      tau: float = 0.0):
+    """Tile-by-tile online-softmax replay of ONE head.  q, k, v: [N, d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    o = np.empty((N, d), dtype=np.float64)
+    lse = np.empty((N,), dtype=np.float64)
+    _load().oracle_online_replay_f64(
+        _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double), N, d,
+        float(scale), int(causal), int(window), int(BM), int(BN), float(tau),
+        _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    return o, lse
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 array -> uint8 E4M3 codes (RNE, saturating to +-448)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_uint8),
+                                     x.size)
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """uint8 E4M3 codes -> float32 values (exact)."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_decode(c) for c in range(256)], dtype=np.float32)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def quantize_fp8_blockwise(x, block: int = 128):
+    """x: [..., N, d] (bf16 values) -> (x8 uint8 [..., N, d], scales float32 [..., ceil(N/block)])."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu").to(torch.float32).numpy()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    shape = x.shape
+    N, d = shape[-2], shape[-1]
+    BH = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    nblk = (N + block - 1) // block
+    x8 = np.empty(shape, dtype=np.uint8)
+    scales = np.empty(shape[:-2] + (nblk,), dtype=np.float32)
+    _load().oracle_quantize_fp8_blockwise(_ptr(x, ctypes.c_float), _ptr(x8, ctypes.c_uint8),
+                                          _ptr(scales, ctypes.c_float), BH, N, d, int(block))
+    return x8, scales
+
+
+def dequantize(x8, scales, block: int = 128) -> np.ndarray:
+    """x_hat = decode(x8) * scale of its row block, in float64 (exact products)."""
+    x8 = np.asarray(x8, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.float32)
+    vals = e4m3_decode(x8).astype(np.float64)
+    N = x8.shape[-2]
+    row_scale = np.repeat(scales.astype(np.float64), block, axis=-1)[..., :N]
+    return vals * row_scale[..., None]
