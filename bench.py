@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the fused exact-attention forward pass on GB300.
+
+Headline line: attn_fwd_bf16 at B=16, H=16, N=8192, d=128, non-causal, in TFLOP/s
+(4*B*H*N^2*d FLOPs per step; halved for causal).  One step = one launch of the
+fused kernel over the whole batch, inputs resident in HBM (1.6 GB of Q/K/V, far
+larger than the 129 MB L2, so no flush is needed between steps).
+
+Also reported on the same line:
+  roofline      the attention kernel against the measured dense bf16 peak
+  e2e           the same metric through the public API with pinned host buffers,
+                host->device copies of Q/K/V and device->host copies of O and LSE
+                inside the timed region
+  cpu_baseline  the float64 CPU oracle on a bounded sample of the workload
+  clocks        nvidia-smi samples taken during the timed region
+  extra         causal bf16, the FP8 path (quantiser + attention) and the quantiser's GB/s
+
+--impl reference times the oracle (the reference arm of this path) instead.
+Multi-GPU (torchrun, --gpus N): independent replicas, one per GPU, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, H, N, D = 16, 16, 8192, 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+FP8_NOMINAL_RATIO = 2.0  # dense fp8 / dense bf16 tensor rate
+
+
+def flops(b, h, n, d, causal=False):
+    f = 4.0 * b * h * n * n * d
+    return f / 2.0 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "MEASURED_PEAKS.json (measured)"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "profiling-recipe fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_55_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.out = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = ["-i", str(device_index)]
+
+    def start(self):
+        try:
+            self.out = open("/tmp/bench_clocks.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open("/tmp/bench_clocks.csv") as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def time_steps(fn, steps, warmup, stream):
+    """CUDA-event time of `steps` calls of fn() on `stream` after `warmup` calls.
+    Returns (total_ms, per_step_ms list)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for s, e in ev:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in ev]
+    total = ev[0][0].elapsed_time(ev[-1][1])
+    return total, per
+
+
+def cpu_baseline(q, k, v, scale, budget_s=12.0):
+    """Time the float64 oracle on a bounded sample of query rows of head (0, 0)."""
+    import numpy as np
+    import oracle
+    qh = q[0, 0].double().numpy()
+    kh = k[0, 0].double().numpy()
+    vh = v[0, 0].double().numpy()
+    n = qh.shape[0]
+    rows = np.arange(0, 64)
+    t0 = time.perf_counter()
+    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows, scale, return_threads=True)
+    t_probe = time.perf_counter() - t0
+    R = int(min(n, max(64, 64 * budget_s / max(t_probe, 1e-3))))
+    rows = np.linspace(0, n - 1, R).astype(np.int64)
+    t0 = time.perf_counter()
+    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows, scale, return_threads=True)
+    dt = time.perf_counter() - t0
+    f = 4.0 * R * n * q.shape[-1]
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": int(nt), "kind": "oracle",
+            "sample": f"{R} query rows of head (0,0) against all {n} keys, d={q.shape[-1]}, "
+                      f"non-causal, float64 ({dt:.1f} s)"}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl != "reference" else "gloo")
+        if args.impl != "reference":
+            torch.cuda.set_device(local)
+    elif args.impl != "reference":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the float64 oracle on host cores, bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from exact_attention_55_gb300.inputs import make_qkv
+    oracle.build()
+    # one head of the headline workload (same seed and recipe)
+    q, k, v = make_qkv(1, 1, N, D, seed=0)
+    scale = 1.0 / math.sqrt(D)
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
+    total_steps = args.steps + args.warmup
+    per_step_budget = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
+    t0 = time.perf_counter()
+    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, np.arange(32), scale, return_threads=True)
+    probe = time.perf_counter() - t0
+    R = int(min(N, max(8, 32 * per_step_budget / max(probe, 1e-4))))
+    rows = np.linspace(0, N - 1, R).astype(np.int64)
+    for _ in range(args.warmup):
+        oracle.attn_rows_f64(qh, kh, vh, rows, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attn_rows_f64(qh, kh, vh, rows, scale)
+    dt = time.perf_counter() - t0
+    f = 4.0 * R * N * D * args.steps
+    value = f / dt / 1e12
+    sample = f"{R} query rows of head (0,0) of B16 H16 N8192 d128 per step, float64"
+    line = {
+        "impl": "reference", "metric": "attention fwd TFLOP/s (bf16 workload)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(False),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_config(causal):
+    return {"workload": f"attention forward bf16 B{B} H{H} N{N} d{D} "
+                        f"{'causal' if causal else 'non-causal'}",
+            "B": B, "H": H, "N": N, "d": D, "causal": causal, "window": 0,
+            "l2": "inputs (1.6 GB Q/K/V) larger than the 129 MB L2; no flush"}
+
+
+def run_gb300(args, world, rank, local):
+    import torch
+    import exact_attention_55_gb300 as fa
+    from exact_attention_55_gb300.inputs import make_qkv
+
+    fa.build.build()
+    fa.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    scale = 1.0 / math.sqrt(D)
+
+    q, k, v = make_qkv(B, H, N, D, seed=0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def step():
+        fa.attn_fwd_bf16(qd, kd, vd, scale=scale, causal=False, o=o, lse=lse, stream=stream)
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.start()
+    total_ms, per = time_steps(step, args.steps, 0, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    status = fa.attn_get_device_status()
+    if status != fa.ATTN_OK:
+        raise RuntimeError(f"device status {status} after the timed region")
+    total_ms = max_over_ranks(total_ms, world)
+    f_step = flops(B, H, N, D)
+    value = world * args.steps * f_step / (total_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(per)
+    achieved = f_step / (avg_launch_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "traffic": profiled_traffic("attn_fwd_bf16_d128_headline"),
+                "kernel": "attn_fwd_kernel<128,bf16>",
+                "peak_source": peak_src + " bf16 burst (cuBLAS 8192^3)",
+                "flops_per_launch": f_step}
+
+    extra = {}
+    if rank == 0 and not args.quick:
+        extra = measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks)
+
+    # e2e through the public API with pinned host buffers
+    e2e = None
+    if not args.quick:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            fa.attn_fwd_bf16(qd, kd, vd, scale=scale, o=o, lse=lse, stream=stream)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(world)
+        e2e_ms, _ = time_steps(e2e_step, n_e2e, 2, stream)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": world * n_e2e * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * q.numel() * 2,
+               "d2h_bytes_per_step": q.numel() * 2 + B * H * N * 4,
+               "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and not args.quick:
+        cpu = cpu_baseline(q, k, v, scale)
+
+    if rank == 0:
+        line = {
+            "metric": "attention fwd TFLOP/s (bf16, fp8) at B16 H16 N8192 d128; % of TC peak",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(False),
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+            "gpu_launches": args.steps, "extra": extra,
+        }
+        print(json.dumps(line))
+
+
+def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
+    """Causal bf16, the FP8 path and the quantiser on the same device."""
+    import torch
+    from exact_attention_55_gb300.inputs import make_qkv
+    out = {}
+    reps = max(5, min(args.steps, 30))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def causal_step():
+        fa.attn_fwd_bf16(qd, kd, vd, scale=scale, causal=True, o=o, lse=lse, stream=stream)
+
+    ms, per = time_steps(causal_step, reps, 3, stream)
+    f = flops(B, H, N, D, causal=True)
+    out["bf16_causal"] = {"tflops": f / (statistics.mean(per) * 1e-3) / 1e12,
+                          "ms": statistics.mean(per)}
+
+    # FP8 workload: outliers, per-128-row-block quantisation, FP8 attention
+    q2, k2, v2 = make_qkv(B, H, N, D, seed=0, outliers=True)
+    q2d, k2d, v2d = q2.to(dev), k2.to(dev), v2.to(dev)
+    del q2, k2, v2
+    nb = N // 128
+    bufs = [(torch.empty(q2d.shape, dtype=torch.uint8, device=dev),
+             torch.empty((B, H, nb), dtype=torch.float32, device=dev)) for _ in range(3)]
+
+    def quant_step():
+        for x, (x8, sc) in zip((q2d, k2d, v2d), bufs):
+            fa.attn_quantize_fp8_blockwise(x, x8=x8, scales=sc, stream=stream)
+
+    ms, per = time_steps(quant_step, reps, 3, stream)
+    qbytes = 3 * (q2d.numel() * 3 + B * H * nb * 4)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = qbytes / (statistics.mean(per) * 1e-3) / 1e9
+    out["quantize_fp8"] = {"GB_per_s": gbs, "ms_3_tensors": statistics.mean(per),
+                           "frac_of_hbm": gbs / hbm, "bytes": qbytes}
+    (q8, sq), (k8, sk), (v8, sv) = bufs
+    peak8 = float(peaks.get("fp8_tflops",
+                            FP8_NOMINAL_RATIO * float(peaks.get("bf16_tflops", 1900.0))))
+    for causal in (False, True):
+        def fp8_step():
+            fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, scale=scale, causal=causal, o=o, lse=lse,
+                            stream=stream)
+        ms, per = time_steps(fp8_step, reps, 3, stream)
+        f = flops(B, H, N, D, causal=causal)
+        t = f / (statistics.mean(per) * 1e-3) / 1e12
+        out["fp8_causal" if causal else "fp8"] = {
+            "tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
+            "peak": peak8, "peak_source": "fp8 = 2 x measured bf16 burst (nominal ratio)"}
+    status = fa.attn_get_device_status()
+    out["device_status"] = status
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gb300(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

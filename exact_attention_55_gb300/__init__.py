@@ -1,0 +1,173 @@
+"""GB300 (sm_103a) fused exact-attention forward: thin Python binding of the C ABI.
+
+The functions below carry the C entry points' names (``include/attn.h``) and do
+argument marshalling only: every arithmetic step runs in the CUDA library
+``_build/libgb300attn.so``.  PyTorch supplies device memory and the stream.
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+
+    import exact_attention_55_gb300 as fa
+    o, lse = fa.attn_fwd_bf16(q, k, v, causal=True)          # q, k, v: cuda bf16 [B,H,N,d]
+    q8, sq = fa.attn_quantize_fp8_blockwise(q)               # E4M3 codes + per-block scales
+    o8, lse8 = fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
+    "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
+    "attn_get_device_status", "EXPORTED_SYMBOLS",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+
+EXPORTED_SYMBOLS = (
+    "attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
+    "attn_get_device_status",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of the CUDA library.  Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library not built: {path} is missing (run exact_attention_55_gb300.build.build())")
+        lib = ctypes.CDLL(path)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.attn_fwd_bf16.restype = i
+        lib.attn_quantize_fp8_blockwise.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.attn_quantize_fp8_blockwise.restype = i
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.attn_fwd_fp8.restype = i
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_get_device_status.argtypes = [vp]
+        lib.attn_get_device_status.restype = i
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check_bhnd(name, t, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+
+
+def _raise_if(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def attn_fwd_bf16(q, k, v, scale: float | None = None, causal: bool = False, window: int = 0,
+                  o=None, lse=None, stream=None):
+    """O = softmax(scale * Q K^T + mask) V and the natural-log LSE; bf16 in and out."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bhnd(n, t, torch.bfloat16)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_bhnd("o", o, torch.bfloat16)
+    st = load_library().attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                      int(window), _stream_handle(stream))
+    _raise_if(st, "attn_fwd_bf16")
+    return o, lse
+
+
+def attn_quantize_fp8_blockwise(x, block: int = 128, x8=None, scales=None, stream=None):
+    """Per-(head, 128-row block) E4M3 quantisation; returns (x8 uint8 codes, fp32 scales)."""
+    _check_bhnd("x", x, torch.bfloat16)
+    B, H, N, d = x.shape
+    if x8 is None:
+        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, (N + block - 1) // block), dtype=torch.float32,
+                             device=x.device)
+    st = load_library().attn_quantize_fp8_blockwise(x.data_ptr(), x8.data_ptr(),
+                                                    scales.data_ptr(), B, H, N, d, int(block),
+                                                    _stream_handle(stream))
+    _raise_if(st, "attn_quantize_fp8_blockwise")
+    return x8, scales
+
+
+def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | None = None,
+                 causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
+    """Forward pass on E4M3 operands (uint8 codes or float8_e4m3fn) with per-block descales."""
+    for n, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        _check_bhnd(n, t, torch.uint8)
+    B, H, N, d = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous cuda float32 tensor")
+    st = load_library().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(),
+                                     descale_q.data_ptr(), descale_k.data_ptr(),
+                                     descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,
+                                     d, float(scale), int(bool(causal)), int(window),
+                                     _stream_handle(stream))
+    _raise_if(st, "attn_fwd_fp8")
+    return o, lse
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load_library().attn_get_device_status(_stream_handle(stream)))

@@ -1,0 +1,237 @@
+// api.cu -- the C ABI: argument checks, tensor-map encoding and kernel launches.
+//
+// No entry point allocates device memory or synchronises (except
+// attn_get_device_status, which exists to synchronise).  Tensor maps are encoded
+// on the host for every call (a few microseconds) and passed by value as
+// __grid_constant__ kernel parameters.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "attn_fwd.cuh"
+#include "attn_params.h"
+
+namespace gb300 {
+
+cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream);
+
+// One status word per device: kernels write kStatusTimeout here when they give up.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s per mbarrier wait
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device facts, looked up once with that device current.
+attn_status_t device_info(DeviceInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
+        d.sm_count = sms;
+        d.status = static_cast<int*>(addr);
+        d.ready = true;
+    }
+    if (g_encode == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return ATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = &d;
+    return ATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D map over a [BH, N, d] tensor: dims (d, N, BH) innermost first, 128-byte
+// swizzled boxes of (128 bytes of d) x box_rows x 1.  Rows past N read as zero.
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int d,
+               int N, int BH, int box_rows)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)N * d * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool F8>
+attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const float* dq, const float* dk, const float* dv, int BH, int N, float scale,
+                      int causal, int window, cudaStream_t stream)
+{
+    using C = FwdCfg<D, F8>;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    const CUtensorMapDataType dt =
+        F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    alignas(64) CUtensorMap mq, mk, mv;
+    if (!encode_3d(&mq, q, dt, C::EB, D, N, BH, C::BM) ||
+        !encode_3d(&mk, k, dt, C::EB, D, N, BH, C::BN) ||
+        !encode_3d(&mv, v, dt, C::EB, D, N, BH, C::BN))
+        return ATTN_ERR_CUDA;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.o = o;
+    p.lse = lse;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = dev->status;
+    p.BH = BH;
+    p.N = N;
+    p.num_qblk = (N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+    const long long units = (long long)BH * p.num_qblk;
+    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    p.num_units = (int)units;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    p.timeout_ns = kWaitTimeoutNs;
+    if (launch_attn_fwd<D, F8>(mq, mk, mv, p, dev->sm_count, stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status_t check_common(int B, int H, int N, float scale, long long* BH)
+{
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    *BH = (long long)B * H;
+    if (*BH > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int B, int H, int N, int d, float scale,
+                                       int causal, int window, void* stream)
+{
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    long long BH = 0;
+    attn_status_t st = check_common(B, H, N, scale, &BH);
+    if (st != ATTN_OK) return st;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (d) {
+        case 64: return run_fwd<64, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
+        case 128: return run_fwd<128, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
+        default: return run_fwd<256, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
+    }
+}
+
+extern "C" attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                                      const float* descale_q, const float* descale_k,
+                                      const float* descale_v, void* o, float* lse, int B, int H,
+                                      int N, int d, float scale, int causal, int window,
+                                      void* stream)
+{
+    if (!q8 || !k8 || !v8 || !descale_q || !descale_k || !descale_v || !o || !lse)
+        return ATTN_ERR_INVALID_ARG;
+    long long BH = 0;
+    attn_status_t st = check_common(B, H, N, scale, &BH);
+    if (st != ATTN_OK) return st;
+    if ((d != 128 && d != 256) || N % 128 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(descale_q, 4) || !aligned(descale_k, 4) ||
+        !aligned(descale_v, 4))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 128)
+        return run_fwd<128, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s);
+    return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s);
+}
+
+extern "C" attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales, int B,
+                                                     int H, int N, int d, int block, void* stream)
+{
+    if (!x || !x8 || !scales) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+    if (block != 128 || d % 16 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scales, 4)) return ATTN_ERR_MISALIGNED;
+    const long long BH = (long long)B * H;
+    const long long nblk = (N + 127) / 128;
+    if (BH * nblk > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    QuantParams p;
+    p.x = x;
+    p.x8 = static_cast<uint8_t*>(x8);
+    p.scales = scales;
+    p.BH = (int)BH;
+    p.N = N;
+    p.d = d;
+    p.nblk = (int)nblk;
+    if (launch_quant_fp8(p, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+extern "C" const char* attn_status_string(attn_status_t status)
+{
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+        case ATTN_ERR_MISALIGNED: return "misaligned pointer";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "kernel gave up on an internal wait";
+        default: return "unknown status";
+    }
+}
+
+extern "C" attn_status_t attn_get_device_status(void* stream)
+{
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpy(&value, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return value == 0 ? ATTN_OK : static_cast<attn_status_t>(value);
+}

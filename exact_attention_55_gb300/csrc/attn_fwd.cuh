@@ -1,0 +1,586 @@
+// attn_fwd.cuh -- fused exact-attention forward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Computes, per head, O = softmax(scale * Q K^T + mask) V and the per-row
+// log-sum-exp, block by block with an online softmax so the N x N scores never
+// leave the SM.  Pages it follows (titles as published):
+//   [WGC] "Warp Group Cluster 优化：Flash Attention V3 在 H100 上的 FP8 融合计算实践"
+//         §2 GEMM-Softmax 融合流水线 (local max/sum, running statistics, rescale,
+//         straight into the next GEMM), §3 FP8 量化与精度保持 (per-block scaling,
+//         FP32 accumulation, 16-bit output), 运行时调优 (128-row Q tiles, 3-4 stage pipeline)
+//   [JJ]  "大模型加速-核心网络算子-Flash Attention V3"
+//         §2.1 producer/consumer warp specialisation and ping-pong of two softmax
+//         groups against the GEMMs, §2.2 softmax overlapped with the asynchronous
+//         GEMMs, §1.1 TMA block copies, §2.4 (first) transaction-count barriers
+//   [YT]  "FlashAttention V3：优化框架吞吐量的关键技术实践"
+//         §1.2 mask fused with matmul and softmax, §2.1.2 band-mask zero-region skipping
+//
+// Blackwell design (not a port of the Hopper one on the pages):
+//   * one persistent CTA per SM walks work units (head, 128*NQ query rows);
+//   * warp PRODUCER (one lane) streams Q tiles and K/V tiles with TMA into a
+//     ring of NSLOT shared-memory slots, each guarded by a full/empty mbarrier;
+//   * warp MMA (one lane) issues tcgen05.mma: S = Q K^T into tensor memory, and
+//     O += P V with P read back from tensor memory (it overwrites S in place);
+//   * NQ softmax warpgroups (one thread = one query row) read S from TMEM,
+//     apply the mask on edge tiles, update the running max with a lazy
+//     threshold, exponentiate with ex2, keep the running sum, write P to TMEM
+//     and, only when the stale maximum would let P exceed 2^tau, rescale their
+//     O rows in TMEM; at the end they normalise O and write O and the LSE.
+//   With NQ = 2 the two Q tiles ping-pong: one group's softmax runs while the
+//   tensor core works on the other tile's GEMMs.  With NQ = 1 (d = 256) S is
+//   double-buffered so QK^T of the next block overlaps the current softmax.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "attn_params.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+template <int D, bool F8>
+struct FwdCfg {
+    static constexpr int BM = 128;                       // query rows per Q tile (MMA M)
+    static constexpr int NQ = (D <= 128) ? 2 : 1;        // Q tiles per work unit
+    static constexpr int BN = (D == 256 && !F8) ? 64 : 128;  // keys per K/V tile
+    static constexpr int EB = F8 ? 1 : 2;                // bytes per operand element
+    static constexpr int SWE = 128 / EB;                 // elements per 128-byte swizzle row
+    static constexpr int NCB = D / SWE;                  // 128-byte column blocks per row
+    static constexpr int CB_Q_BYTES = BM * 128;
+    static constexpr int CB_KV_BYTES = BN * 128;
+    static constexpr int Q_BYTES = NCB * CB_Q_BYTES;
+    static constexpr int KV_BYTES = NCB * CB_KV_BYTES;
+    static constexpr int SMEM_CAP = 227 * 1024;
+    static constexpr int BAR_BYTES = 1024;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - NQ * Q_BYTES) / KV_BYTES;
+    static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
+    static constexpr int SMEM_BYTES = ALIGN_SLACK + NQ * Q_BYTES + NSLOT * KV_BYTES + BAR_BYTES;
+    static constexpr int K_STEP = F8 ? 32 : 16;          // K per tcgen05.mma
+    static constexpr int NSB = 2;                        // S/P buffers in TMEM
+    static constexpr int S_COL0 = 0;                     // S buffer b at columns [b*BN, b*BN+BN)
+    static constexpr int O_COL0 = NSB * BN;              // O of Q tile i at [O_COL0 + i*D, +D)
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int P_COLS = BN * EB / 4;           // packed P columns (2 bf16 / 4 e4m3 per col)
+    static constexpr int NUM_SOFTMAX_WARPS = 4 * NQ;
+    static constexpr int PRODUCER_WARP = NUM_SOFTMAX_WARPS;   // first warp of the last warpgroup
+    static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
+    static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + 4);  // whole warpgroups
+    // Register split (NQ = 2 only): softmax warpgroups grow, the control warpgroup
+    // shrinks.  Needs REG_POOL <= registers per thread at launch * NUM_THREADS.
+    static constexpr bool SPLIT_REGS = NQ == 2;
+    static constexpr int REG_SOFTMAX = 208;
+    static constexpr int REG_CONTROL = 88;
+    static constexpr int REG_POOL = NQ * 128 * REG_SOFTMAX + 128 * REG_CONTROL;
+    // bf16: lazy-rescale threshold in log2 units (P <= 2^TAU while the max is stale).
+    // fp8: the running max is always exact (P <= 1) and O is rescaled every key tile
+    // anyway, because the V descale of tile t is applied to O, not folded into P.
+    static constexpr float TAU = 8.0f;
+    // fp8: P is stored as e4m3(p * 2^P8_SHIFT); a power of two keeps p = 1 exact.
+    static constexpr int P8_SHIFT = 8;
+
+    static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static_assert(!F8 || D >= 128, "fp8 needs a full 128-byte row");
+    static_assert(NSLOT >= 3, "ring too small");
+    static_assert(O_COL0 + NQ * D <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory budget");
+    static_assert(BN % 32 == 0 && D % 32 == 0, "chunking");
+};
+
+// Shared-memory barrier block (lives in the last BAR_BYTES of dynamic smem).
+struct alignas(8) FwdBars {
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t o_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct Unit {
+    int bh;      // flattened (batch, head)
+    int q0;      // first query row of the unit
+    int t0;      // first key tile
+    int n;       // key tiles visited
+};
+
+// Work unit u -> (head, query block, key-tile range).  Units of one head are
+// adjacent so concurrently running CTAs share that head's K/V in L2; with a
+// causal or banded mask the query blocks of a head run last-first so the
+// longest units start first.
+template <class C>
+__device__ __forceinline__ Unit unit_of(int u, const FwdParams& p)
+{
+    Unit w;
+    w.bh = u / p.num_qblk;
+    int qb = u % p.num_qblk;
+    if (p.causal || p.window > 0) qb = p.num_qblk - 1 - qb;
+    w.q0 = qb * (C::NQ * C::BM);
+    const int r_last = min(p.N, w.q0 + C::NQ * C::BM) - 1;
+    int lo = 0, hi = p.N;  // keys [lo, hi) that some row of the unit may use
+    if (p.window > 0) lo = max(0, w.q0 - p.window);
+    if (p.causal) hi = r_last + 1;
+    else if (p.window > 0) hi = min(p.N, r_last + p.window + 1);
+    w.t0 = lo / C::BN;
+    w.n = (hi + C::BN - 1) / C::BN - w.t0;
+    return w;
+}
+
+__device__ __forceinline__ void raise_timeout(const FwdParams& p, FwdBars* bars)
+{
+    atomicExch(p.status, kStatusTimeout);
+    *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
+}
+
+template <int D, bool F8>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p)
+{
+    using C = FwdCfg<D, F8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* q_smem = smem;                                   // NQ tiles
+    uint8_t* kv_smem = smem + C::NQ * C::Q_BYTES;             // NSLOT tiles
+    FwdBars* bars = reinterpret_cast<FwdBars*>(kv_smem + C::NSLOT * C::KV_BYTES);
+    const volatile int* abort_flag = &bars->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&bars->q_full[i]), 1);
+            mbar_init(smem_u32(&bars->q_empty[i]), 1);
+            mbar_init(smem_u32(&bars->s_full[i]), 1);
+            mbar_init(smem_u32(&bars->p_full[i]), 4);
+            mbar_init(smem_u32(&bars->pv_done[i]), 1);
+            mbar_init(smem_u32(&bars->o_empty[i]), 4);
+        }
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(smem_u32(&bars->kv_full[s]), 1);
+            mbar_init(smem_u32(&bars->kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == C::MMA_WARP) {
+        tmem_alloc(smem_u32(&bars->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    if (warp == C::PRODUCER_WARP) {
+        // ------------------------------------------------------------ TMA producer
+        if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+            uint32_t ring = 0, uc = 0;
+            uint32_t q_armed[2] = {0, 0};
+            bool ok = true;
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+                const Unit w = unit_of<C>(u, p);
+                for (int i = 0; i < C::NQ && ok; ++i) {
+                    const uint32_t fb = smem_u32(&bars->q_full[i]);
+                    if (!mbar_wait(smem_u32(&bars->q_empty[i]), (uc & 1) ^ 1, abort_flag,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(fb, C::Q_BYTES);
+                    ++q_armed[i];
+                    const uint32_t dst = smem_u32(q_smem + i * C::Q_BYTES);
+#pragma unroll
+                    for (int cb = 0; cb < C::NCB; ++cb)
+                        tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE,
+                                    w.q0 + i * C::BM, w.bh, pol_q);
+                }
+                for (int jj = 0; jj < w.n && ok; ++jj) {
+                    const int c0 = (w.t0 + jj) * C::BN;
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {  // K then V
+                        const uint32_t slot = ring % C::NSLOT;
+                        const uint32_t par = ((ring / C::NSLOT) & 1) ^ 1;
+                        if (!mbar_wait(smem_u32(&bars->kv_empty[slot]), par, abort_flag,
+                                       p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = smem_u32(&bars->kv_full[slot]);
+                        mbar_arrive_expect_tx(fb, C::KV_BYTES);
+                        const uint32_t dst = smem_u32(kv_smem + slot * C::KV_BYTES);
+                        const CUtensorMap* map = which == 0 ? &tmK : &tmV;
+#pragma unroll
+                        for (int cb = 0; cb < C::NCB; ++cb)
+                            tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, c0,
+                                        w.bh, pol_kv);
+                        ++ring;
+                    }
+                }
+            }
+            if (!ok) {
+                raise_timeout(p, bars);
+                // Let every copy already issued land before shared memory is released:
+                // the latest arming of each ring slot and of each Q buffer.
+                const uint32_t armed = ring < C::NSLOT ? ring : C::NSLOT;
+                for (uint32_t k = ring - armed; k < ring; ++k)
+                    mbar_wait(smem_u32(&bars->kv_full[k % C::NSLOT]), (k / C::NSLOT) & 1,
+                              nullptr, p.timeout_ns);
+                for (int i = 0; i < C::NQ; ++i)
+                    if (q_armed[i] > 0)
+                        mbar_wait(smem_u32(&bars->q_full[i]), (q_armed[i] - 1) & 1, nullptr,
+                                  p.timeout_ns);
+            }
+        }
+    } else if (warp == C::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer
+        if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
+        if (lane == 0) {
+            constexpr uint32_t fmt = F8 ? 0u : 1u;
+            constexpr uint32_t idesc_s = idesc_f32acc(fmt, 0, C::BM, C::BN);
+            constexpr uint32_t idesc_o = idesc_f32acc(fmt, 1, C::BM, D);
+            const uint32_t q_base = smem_u32(q_smem);
+            const uint32_t kv_base = smem_u32(kv_smem);
+            uint32_t ring = 0, uc = 0;
+            uint32_t p_phase = 0;  // bit b: parity of the next p_full[b] completion
+            bool ok = true;
+
+            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+                if (!ok) return false;
+                if (!mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns)) ok = false;
+                return ok;
+            };
+            // S[sb] = Q_i K^T with K in ring slot `slot`
+            auto issue_s = [&](int i, int sb, uint32_t slot) {
+                const uint32_t a0 = q_base + i * C::Q_BYTES;
+                const uint32_t b0 = kv_base + slot * C::KV_BYTES;
+                const uint32_t d_t = tmem + C::S_COL0 + sb * C::BN;
+#pragma unroll
+                for (int kk = 0; kk < D / C::K_STEP; ++kk) {
+                    const int byte = kk * C::K_STEP * C::EB;  // offset along the row
+                    const uint32_t off_a = (byte / 128) * C::CB_Q_BYTES + (byte % 128);
+                    const uint32_t off_b = (byte / 128) * C::CB_KV_BYTES + (byte % 128);
+                    mma_ss<F8>(d_t, sdesc_sw128(a0 + off_a, 16, 1024),
+                               sdesc_sw128(b0 + off_b, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_i (+)= P[sb] V with V in ring slot `slot` (V is MN-major: d contiguous)
+            auto issue_pv = [&](int i, int sb, uint32_t slot, bool accumulate) {
+                const uint32_t b0 = kv_base + slot * C::KV_BYTES;
+                const uint32_t d_t = tmem + C::O_COL0 + i * D;
+                const uint32_t a_t = tmem + C::S_COL0 + sb * C::BN;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / C::K_STEP; ++kk) {
+                    const uint32_t off_b = kk * C::K_STEP * 128;  // K_STEP key rows of 128 B
+                    mma_ts<F8>(d_t, a_t + kk * (C::K_STEP * C::EB / 4),
+                               sdesc_sw128(b0 + off_b, C::CB_KV_BYTES, 1024), idesc_o,
+                               (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+                const Unit w = unit_of<C>(u, p);
+                for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
+                tc_fence_after_sync();
+                // step 0: S(0) for every Q tile
+                {
+                    const uint32_t slot = ring % C::NSLOT;
+                    if (!wait(&bars->kv_full[slot], (ring / C::NSLOT) & 1)) break;
+                    for (int i = 0; i < C::NQ; ++i) {
+                        issue_s(i, i, slot);
+                        mma_commit(smem_u32(&bars->s_full[i]));
+                        if (w.n == 1) mma_commit(smem_u32(&bars->q_empty[i]));
+                    }
+                    mma_commit(smem_u32(&bars->kv_empty[slot]));
+                    ++ring;
+                }
+                for (int jj = 1; jj < w.n && ok; ++jj) {
+                    const uint32_t slot_v = ring % C::NSLOT;         // V_{jj-1}
+                    const uint32_t slot_k = (ring + 1) % C::NSLOT;   // K_jj
+                    const uint32_t par_v = (ring / C::NSLOT) & 1;
+                    const uint32_t par_k = ((ring + 1) / C::NSLOT) & 1;
+                    if constexpr (C::NQ == 2) {
+                        if (!wait(&bars->kv_full[slot_v], par_v)) break;
+                        for (int i = 0; i < 2; ++i) {
+                            if (!wait(&bars->p_full[i], (p_phase >> i) & 1)) break;
+                            p_phase ^= 1u << i;
+                            if (jj == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
+                            tc_fence_after_sync();
+                            issue_pv(i, i, slot_v, jj > 1);
+                            mma_commit(smem_u32(&bars->pv_done[i]));
+                            if (i == 0 && !wait(&bars->kv_full[slot_k], par_k)) break;
+                            issue_s(i, i, slot_k);
+                            mma_commit(smem_u32(&bars->s_full[i]));
+                            if (jj == w.n - 1) mma_commit(smem_u32(&bars->q_empty[i]));
+                        }
+                    } else {
+                        const int sb = jj & 1, sp = (jj - 1) & 1;
+                        if (!wait(&bars->kv_full[slot_k], par_k)) break;
+                        issue_s(0, sb, slot_k);
+                        mma_commit(smem_u32(&bars->s_full[sb]));
+                        if (jj == w.n - 1) mma_commit(smem_u32(&bars->q_empty[0]));
+                        if (!wait(&bars->kv_full[slot_v], par_v)) break;
+                        if (!wait(&bars->p_full[sp], (p_phase >> sp) & 1)) break;
+                        p_phase ^= 1u << sp;
+                        if (jj == 1 && !wait(&bars->o_empty[0], (uc & 1) ^ 1)) break;
+                        tc_fence_after_sync();
+                        issue_pv(0, sp, slot_v, jj > 1);
+                        mma_commit(smem_u32(&bars->pv_done[0]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars->kv_empty[slot_v]));
+                    mma_commit(smem_u32(&bars->kv_empty[slot_k]));
+                    ring += 2;
+                }
+                if (!ok) break;
+                // tail: P(n-1) V_{n-1}
+                {
+                    const uint32_t slot_v = ring % C::NSLOT;
+                    if (!wait(&bars->kv_full[slot_v], (ring / C::NSLOT) & 1)) break;
+                    const int sp = (C::NQ == 2) ? 0 : ((w.n - 1) & 1);
+                    for (int i = 0; i < C::NQ; ++i) {
+                        const int sb = (C::NQ == 2) ? i : sp;
+                        if (!wait(&bars->p_full[sb], (p_phase >> sb) & 1)) break;
+                        p_phase ^= 1u << sb;
+                        if (w.n == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
+                        tc_fence_after_sync();
+                        issue_pv(i, sb, slot_v, w.n > 1);
+                        mma_commit(smem_u32(&bars->pv_done[i]));
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&bars->kv_empty[slot_v]));
+                    ++ring;
+                }
+            }
+            if (!ok) raise_timeout(p, bars);
+            // Drain: every MMA this thread issued has finished before TMEM is freed.
+            mma_commit(smem_u32(&bars->drain));
+            mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp < C::NUM_SOFTMAX_WARPS) {
+        // ------------------------------------------------------------ softmax groups
+        if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
+        const int grp = warp >> 2;           // Q tile of this warpgroup
+        const int wq = warp & 3;             // TMEM lane quarter
+        const int row_in_tile = wq * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        uint32_t s_phase = 0, pv_phase = 0;  // per-buffer / per-tile parities
+        uint32_t uc = 0;
+        bool ok = true;
+
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
+            r = __all_sync(0xffffffffu, r);
+            if (!r) ok = false;
+            return r;
+        };
+
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+            const Unit w = unit_of<C>(u, p);
+            const int a = w.q0 + grp * C::BM;    // first row of this Q tile
+            const int row = a + row_in_tile;     // this thread's query row
+            // keys allowed for this row: [jlo, jhi]
+            int jlo = 0, jhi = p.N - 1;
+            if (p.causal) jhi = min(jhi, row);
+            if (p.window > 0) {
+                jlo = row - p.window;
+                if (!p.causal) jhi = min(jhi, row + p.window);
+            }
+            // fp8: O is kept in units of the current key tile's V descale: before
+            // P(t) V8(t) is added, O *= alpha * dv(t-1) / dv(t).
+            float dv_cur = 1.0f, q_desc = 1.0f;
+            if constexpr (F8) q_desc = p.dq[(size_t)w.bh * ((p.N + 127) / 128) + a / 128];
+
+            float m_used = NEG_INF, l = 0.0f;
+            for (int jj = 0; jj < w.n; ++jj) {
+                const int t = w.t0 + jj;
+                const int c0 = t * C::BN;
+                const int sb = (C::NQ == 2) ? grp : (jj & 1);
+                float c = p.c_log2;
+                float dv_ratio = 1.0f;  // fp8: dv(t-1) / dv(t)
+                if constexpr (F8) {
+                    const int nkb = (p.N + 127) / 128;
+                    c = p.c_log2 * q_desc * p.dk[(size_t)w.bh * nkb + t];
+                    const float dv_t = p.dv[(size_t)w.bh * nkb + t];
+                    dv_ratio = dv_cur / dv_t;
+                    dv_cur = dv_t;
+                }
+                if (!wait_all(&bars->s_full[sb], (s_phase >> sb) & 1)) break;
+                s_phase ^= 1u << sb;
+                tc_fence_after_sync();
+
+                float s[C::BN];
+                const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + sb * C::BN;
+#pragma unroll
+                for (int ch = 0; ch < C::BN / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(s_addr + ch * 32, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(r[e]);
+                }
+                // mask only on tiles that cross a boundary of some row's allowed set
+                const bool edge = (c0 + C::BN > p.N) || (p.causal && c0 + C::BN - 1 > a) ||
+                                  (p.window > 0 &&
+                                   (c0 < a + C::BM - 1 - p.window ||
+                                    (!p.causal && c0 + C::BN - 1 > a + p.window)));
+                if (edge) {
+#pragma unroll
+                    for (int e = 0; e < C::BN; ++e) {
+                        const int j = c0 + e;
+                        if (j < jlo || j > jhi) s[e] = NEG_INF;
+                    }
+                }
+                float tmax = s[0];
+#pragma unroll
+                for (int e = 1; e < C::BN; ++e) tmax = fmaxf(tmax, s[e]);
+                const float m_cand = tmax * c;
+                const float m_new = fmaxf(m_used, m_cand);
+                // bf16: move the max only when it grew by more than TAU; fp8: always
+                const bool resc = F8 ? (m_new > m_used) : (m_cand > m_used + C::TAU);
+                const float alpha = resc ? ex2(m_used - m_new) : 1.0f;  // ex2(-inf) = 0
+                bool any_resc = false;
+                if (jj > 0) {
+                    any_resc = F8 ? true : __any_sync(0xffffffffu, resc);
+                    if (any_resc) {
+                        // O must hold P(jj-1) V before it is rescaled
+                        if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
+                        pv_phase ^= 1u << grp;
+                        tc_fence_after_sync();
+                        const float f = alpha * dv_ratio;
+                        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
+#pragma unroll
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + ch * 32, r);
+                            tmem_wait_ld(r);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                            tmem_st32(o_addr + ch * 32, r);
+                        }
+                    }
+                }
+                if (resc) {
+                    l *= alpha;
+                    m_used = m_new;
+                }
+                const float mb = (m_used == NEG_INF) ? 0.0f : m_used;
+                float rowsum = 0.0f;
+                const uint32_t p_addr = tmem + lane_addr + C::S_COL0 + sb * C::BN;
+                if constexpr (!F8) {
+#pragma unroll
+                    for (int ch = 0; ch < C::BN / 64; ++ch) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float p0 = ex2(fmaf(s[ch * 64 + 2 * e], c, -mb));
+                            const float p1 = ex2(fmaf(s[ch * 64 + 2 * e + 1], c, -mb));
+                            rowsum += p0 + p1;
+                            r[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st32(p_addr + ch * 32, r);
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < C::BN / 128; ++ch) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float* sp = &s[ch * 128 + 4 * e];
+                            const float p0 = ex2(fmaf(sp[0], c, -mb));
+                            const float p1 = ex2(fmaf(sp[1], c, -mb));
+                            const float p2 = ex2(fmaf(sp[2], c, -mb));
+                            const float p3 = ex2(fmaf(sp[3], c, -mb));
+                            rowsum += (p0 + p1) + (p2 + p3);
+                            constexpr float ps = float(1u << C::P8_SHIFT);
+                            const uint32_t lo = pack_e4m3x2(p0 * ps, p1 * ps);
+                            const uint32_t hi = pack_e4m3x2(p2 * ps, p3 * ps);
+                            r[e] = lo | (hi << 16);
+                        }
+                        tmem_st32(p_addr + ch * 32, r);
+                    }
+                }
+                l += rowsum;
+                tmem_wait_st();
+                if (jj > 0 && !any_resc) {
+                    if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
+                    pv_phase ^= 1u << grp;
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[sb]));
+            }
+            if (!ok) break;
+            // epilogue: O / l -> bf16, LSE
+            if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
+            pv_phase ^= 1u << grp;
+            tc_fence_after_sync();
+            float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+            if constexpr (F8) inv_l *= dv_cur * (1.0f / float(1u << C::P8_SHIFT));
+            const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
+            __nv_bfloat16* orow =
+                reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(o_addr + ch * 32, r);
+                tmem_wait_ld(r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                                        __uint_as_float(r[2 * e + 1]) * inv_l);
+                if (row < p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[grp]));
+            if (row < p.N) {
+                const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : NEG_INF;
+                p.lse[(size_t)w.bh * p.N + row] = lse2 * 0.69314718055994531f;
+            }
+        }
+        if (!ok) raise_timeout(p, bars);
+    } else {
+        // ------------------------------------------------------------ spare warps
+        if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace gb300
+
+namespace gb300 {
+
+// Defined once per (D, F8) instantiation in attn_fwd_inst.cu.
+template <int D, bool F8>
+cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            const FwdParams& p, int sm_count, cudaStream_t stream);
+
+}  // namespace gb300

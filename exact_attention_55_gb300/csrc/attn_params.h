@@ -1,0 +1,39 @@
+// attn_params.h -- launch parameters shared by the host launcher and the kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace gb300 {
+
+// Status codes written to the device status word (same values as attn_status_t).
+enum : int {
+    kStatusOk = 0,
+    kStatusTimeout = 5,
+};
+
+struct FwdParams {
+    void* o;              // bf16 [BH, N, D]
+    float* lse;           // fp32 [BH, N], natural log
+    const float* dq;      // fp8 path: Q descale per (head, 128-row block), else null
+    const float* dk;      // fp8 path: K descale
+    const float* dv;      // fp8 path: V descale
+    int* status;          // device status word (timeouts)
+    int BH;               // batch * heads
+    int N;                // sequence length (queries = keys)
+    int num_qblk;         // query blocks per head (NQ * 128 rows each)
+    int num_units;        // BH * num_qblk
+    int causal;           // 1: key j allowed only for j <= i
+    int window;           // > 0: band of that half-width (left edge only when causal)
+    float c_log2;         // softmax scale * log2(e)
+    unsigned long long timeout_ns;  // bound on every mbarrier wait
+};
+
+struct QuantParams {
+    const void* x;        // bf16 [BH, N, d]
+    uint8_t* x8;          // e4m3 [BH, N, d]
+    float* scales;        // fp32 [BH, ceil(N/128)]
+    int BH, N, d;
+    int nblk;             // ceil(N / 128)
+};
+
+}  // namespace gb300

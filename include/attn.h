@@ -1,0 +1,116 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused exact-attention forward library.
+ *
+ * Pages this interface implements (titles as published):
+ *   [WGC] "Warp Group Cluster 优化：Flash Attention V3 在 H100 上的 FP8 融合计算实践"
+ *   [JJ]  "大模型加速-核心网络算子-Flash Attention V3"
+ *   [YT]  "FlashAttention V3：优化框架吞吐量的关键技术实践"
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are caller-owned DEVICE memory on the current CUDA device, laid out
+ *     [B, H, N, d] contiguous (d innermost, row stride d elements).  q, k, v, o,
+ *     x and x8 must be 16-byte aligned (the kernels move them with TMA or 16-byte
+ *     vectors); lse and scale arrays must be 4-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call only enqueues work on that stream: it never synchronises, never
+ *     allocates device memory, and returns as soon as the launch is queued.
+ *   - Errors are returned as attn_status_t; nothing is launched when a call
+ *     returns anything other than ATTN_OK.  No call throws or exits.
+ *   - The library keeps one device status word per GPU.  A kernel that gives up
+ *     on an internal wait (ATTN_ERR_TIMEOUT) records it there; read it with
+ *     attn_get_device_status().
+ *   - Mask: key j is allowed for query i when 0 <= j < N and
+ *       causal != 0  ->  j <= i
+ *       window  > 0  ->  j >= i - window, and (when causal == 0) j <= i + window
+ *     ([YT] §2.1.2 稀疏性感知的Mask优化 builds the band max(0,i-w) .. i+w; the
+ *     causal band keeps its left edge).  window <= 0 means no window.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* null pointer, B/H/N < 1, scale not finite and > 0 */
+    ATTN_ERR_UNSUPPORTED = 2, /* head dim, block size or sequence length not supported */
+    ATTN_ERR_MISALIGNED = 3,  /* a pointer breaks the alignment rule above */
+    ATTN_ERR_CUDA = 4,        /* the CUDA runtime or driver reported an error */
+    ATTN_ERR_TIMEOUT = 5      /* a kernel gave up on an internal wait (device status only) */
+} attn_status_t;
+
+/*
+ * attn_fwd_bf16 -- O = softmax(scale * Q K^T + mask) V and LSE, bf16 in / bf16 out.
+ *
+ * [WGC] §2 GEMM-Softmax 融合流水线 and [YT] §1.2 (softmax, mask and both matmuls
+ * fused in one kernel, the N x N scores never stored); [JJ] §2.1-2.2 (warp
+ * specialised producer/consumer pipeline, softmax overlapped with the GEMMs).
+ *
+ *   q, k, v : const bf16 [B, H, N, d]
+ *   o       : bf16 [B, H, N, d], written
+ *   lse     : float [B, H, N], written: natural-log log-sum-exp of the masked,
+ *             scaled scores of each query row
+ *   B, H, N : >= 1;  d in {64, 128, 256} (else ATTN_ERR_UNSUPPORTED)
+ *   scale   : finite, > 0 (typically 1/sqrt(d))
+ *   causal, window : mask, see above
+ * Accumulation is fp32 (scores, running max/sum, O); P is rounded to bf16 for
+ * the second matmul.
+ */
+attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int N, int d, float scale, int causal, int window,
+                            void* stream);
+
+/*
+ * attn_quantize_fp8_blockwise -- per-block FP8-E4M3 quantisation.
+ *
+ * [WGC] §3 FP8 量化与精度保持 (per-block dynamic scale onto the FP8 range, whose
+ * largest magnitude is 448); [JJ] §1.5 低精度FP8 (E4M3: 4 exponent, 3 mantissa
+ * bits) and §1 item 3 (块量化).  For each head and each block of `block`
+ * consecutive rows (all d columns):
+ *     amax = max |x|,  scale = amax / 448 (IEEE fp32; 1 when amax == 0),
+ *     x8   = E4M3(x / scale) with IEEE fp32 division, round-to-nearest-even,
+ *            saturating to +-448.
+ *   x      : const bf16 [B, H, N, d]
+ *   x8     : uint8 (E4M3 codes) [B, H, N, d], written
+ *   scales : float [B, H, ceil(N / block)], written; x ~= x8 * scales[block of row]
+ *   block  : must be 128 (else ATTN_ERR_UNSUPPORTED); d % 16 == 0 and d <= 256
+ */
+attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales, int B, int H,
+                                          int N, int d, int block, void* stream);
+
+/*
+ * attn_fwd_fp8 -- the forward pass with both matmuls on FP8-E4M3 operands.
+ *
+ * [WGC] §3 FP8 量化与精度保持 (FP8 inputs, FP32 accumulation, 16-bit output) and
+ * [JJ] §2.3 (FP8 tensor-core GEMMs in the forward pass).
+ *   q8, k8, v8 : const E4M3 [B, H, N, d] as written by attn_quantize_fp8_blockwise
+ *   descale_q/k/v : const float [B, H, N / 128], the matching `scales`
+ *                   (x ~= x8 * descale for the 128-row block of the row)
+ *   o, lse, scale, causal, window : as attn_fwd_bf16
+ *   d in {128, 256}; N % 128 == 0 (else ATTN_ERR_UNSUPPORTED)
+ * Scores are descaled per (query block, key block) inside the softmax; P is
+ * rounded to E4M3 after a per-key-block factor that carries the V descale.
+ */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                           const float* descale_q, const float* descale_k,
+                           const float* descale_v, void* o, float* lse, int B, int H, int N,
+                           int d, float scale, int causal, int window, void* stream);
+
+/* Static English text for a status code (never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then read and clear the status
+ * word of the current device: ATTN_OK, or ATTN_ERR_TIMEOUT when a kernel gave up
+ * on an internal wait since the last read.  Returns ATTN_ERR_CUDA when the
+ * synchronisation itself fails (for instance after a device fault).
+ */
+attn_status_t attn_get_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

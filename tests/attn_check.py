@@ -1,0 +1,61 @@
+"""Shared helpers for the GPU parity tests: oracle evaluation on sampled heads/rows
+and the error measures with the tolerances the tests assert.
+
+Tolerances (fixed by the specification of this path):
+  bf16:  max |dO| <= 1.5e-2, mean |dO| <= 1e-3, max |dLSE| <= 1e-3 (inputs N(0,1))
+  fp8:   RMSE(dO)/RMS(O) <= 1e-2 against the oracle on the dequantised FP8 inputs
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BF16_MAX_ABS = 1.5e-2
+BF16_MEAN_ABS = 1e-3
+LSE_MAX_ABS = 1e-3
+FP8_REL_RMSE_DEQ = 1e-2
+FP8_REL_RMSE_UNQ = 4e-2
+
+
+def oracle_rows(q, k, v, heads, rows, scale, causal, window):
+    """Oracle O [len(heads), R, d] and LSE [len(heads), R] for the given (b, h) heads."""
+    outs, lses = [], []
+    for (b, h) in heads:
+        o, lse = oracle.attn_rows_f64(q[b, h], k[b, h], v[b, h], rows, scale, causal=causal,
+                                      window=window)
+        outs.append(o)
+        lses.append(lse)
+    return np.stack(outs), np.stack(lses)
+
+
+def gather(t, heads, rows):
+    """t: CPU tensor [B, H, N, ...] -> numpy float64 [len(heads), R, ...]."""
+    idx = torch.as_tensor(rows, dtype=torch.long)
+    return np.stack([t[b, h].index_select(0, idx).double().numpy() for (b, h) in heads])
+
+
+def bf16_errors(o_gpu, lse_gpu, o_ref, lse_ref):
+    do = np.abs(o_gpu - o_ref)
+    dl = np.abs(lse_gpu - lse_ref)
+    rms = np.sqrt(np.mean(o_ref ** 2))
+    return {
+        "max_abs_o": float(do.max()),
+        "mean_abs_o": float(do.mean()),
+        "max_abs_lse": float(dl.max()),
+        "rel_rmse_o": float(np.sqrt(np.mean(do ** 2)) / rms) if rms > 0 else 0.0,
+    }
+
+
+def assert_bf16_close(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
+    assert np.isfinite(o_gpu).all() and np.isfinite(lse_gpu).all(), f"{label}: non-finite output"
+    e = bf16_errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    assert e["max_abs_o"] <= BF16_MAX_ABS, f"{label}: {e}"
+    assert e["mean_abs_o"] <= BF16_MEAN_ABS, f"{label}: {e}"
+    assert e["max_abs_lse"] <= LSE_MAX_ABS, f"{label}: {e}"
+    return e
+
+
+def rel_rmse(a, ref):
+    return float(np.sqrt(np.mean((a - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))

@@ -1,0 +1,111 @@
+"""CPU checks of the C ABI: the library loads, exports every function include/attn.h
+declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_55_gb300 import build
+    path = build.build()
+    import exact_attention_55_gb300 as fa
+    return fa.load_library(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8",
+              "attn_status_string", "attn_get_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} is declared in attn.h but not exported"
+
+
+def test_binding_names_match_header():
+    import exact_attention_55_gb300 as fa
+    for name in _declared_functions():
+        assert callable(getattr(fa, name)), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.attn_status_string(code)
+    assert lib.attn_status_string(99) == b"unknown status"
+
+
+P = 0x10000  # a 16-byte aligned fake device address; no call below reaches the GPU
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((0, P, P, P, P, 1, 1, 128, 128, 0.1, 0, 0), 1),          # null q
+    ((P, P, P, P, 0, 1, 1, 128, 128, 0.1, 0, 0), 1),          # null lse
+    ((P, P, P, P, P, 0, 1, 128, 128, 0.1, 0, 0), 1),          # B = 0
+    ((P, P, P, P, P, 1, 1, 0, 128, 0.1, 0, 0), 1),            # N = 0
+    ((P, P, P, P, P, 1, 1, 128, 128, 0.0, 0, 0), 1),          # scale = 0
+    ((P, P, P, P, P, 1, 1, 128, 128, float("nan"), 0, 0), 1),  # scale = nan
+    ((P, P, P, P, P, 1, 1, 128, 128, float("inf"), 0, 0), 1),  # scale = inf
+    ((P, P, P, P, P, 1, 1, 128, 96, 0.1, 0, 0), 2),           # d = 96
+    ((P, P, P, P, P, 1, 1, 128, 32, 0.1, 0, 0), 2),           # d = 32
+    ((P + 8, P, P, P, P, 1, 1, 128, 128, 0.1, 0, 0), 3),      # q misaligned
+    ((P, P, P, P + 2, P, 1, 1, 128, 128, 0.1, 0, 0), 3),      # o misaligned
+    ((P, P, P, P, P + 2, 1, 1, 128, 128, 0.1, 0, 0), 3),      # lse misaligned
+])
+def test_bf16_argument_errors(lib, args, expected):
+    assert lib.attn_fwd_bf16(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((0, P, P, 1, 1, 128, 128, 128), 1),
+    ((P, P, P, 1, 1, 128, 128, 64), 2),      # block != 128
+    ((P, P, P, 1, 1, 128, 120, 128), 2),     # d % 16 != 0
+    ((P, P, P, 1, 1, 128, 512, 128), 2),     # d > 256
+    ((P + 4, P, P, 1, 1, 128, 128, 128), 3),
+    ((P, P, P + 2, 1, 1, 128, 128, 128), 3),
+])
+def test_quantizer_argument_errors(lib, args, expected):
+    assert lib.attn_quantize_fp8_blockwise(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((P, P, P, 0, P, P, P, P, 1, 1, 256, 128, 0.1, 0, 0), 1),   # null descale
+    ((P, P, P, P, P, P, P, P, 1, 1, 200, 128, 0.1, 0, 0), 2),   # N % 128
+    ((P, P, P, P, P, P, P, P, 1, 1, 256, 64, 0.1, 0, 0), 2),    # d = 64
+    ((P, P, P + 1, P, P, P, P, P, 1, 1, 256, 128, 0.1, 0, 0), 3),
+])
+def test_fp8_argument_errors(lib, args, expected):
+    assert lib.attn_fwd_fp8(*args, None) == expected
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import exact_attention_55_gb300 as fa
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fa.attn_fwd_bf16(q, q, q)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import exact_attention_55_gb300 as fa
+    saved = fa._lib
+    fa._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            fa.load_library(str(tmp_path / "nope.so"))
+    finally:
+        fa._lib = saved

@@ -1,0 +1,112 @@
+"""GPU parity of the FP8 path: the block quantiser bit for bit against the oracle's
+quantiser, and attn_fwd_fp8 against the oracle on the dequantised inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_55_gb300.inputs import make_qkv, sampled_heads, sampled_rows
+from tests.attn_check import FP8_REL_RMSE_DEQ, gather, oracle_rows, rel_rmse
+from tests.conftest import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    require_gpu()
+    import exact_attention_55_gb300 as fa
+    fa.load_library()
+    return fa
+
+
+def _quant_gpu(fa, x):
+    x8, sc = fa.attn_quantize_fp8_blockwise(x.cuda())
+    assert fa.attn_get_device_status() == fa.ATTN_OK
+    return x8.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("N,d", [(128, 128), (1000, 64), (1000, 128), (300, 256), (77, 16)])
+def test_quantizer_bit_exact_small(fa, N, d):
+    q, k, v = make_qkv(2, 3, N, d, seed=21, outliers=True)
+    for x in (q, k, v):
+        x8, sc = _quant_gpu(fa, x)
+        r8, rsc = oracle.quantize_fp8_blockwise(x, 128)
+        np.testing.assert_array_equal(sc, rsc)
+        np.testing.assert_array_equal(x8, r8)
+
+
+def test_quantizer_zero_block(fa):
+    x = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16)
+    x[0, 0, 200, 5] = 3.0
+    x8, sc = _quant_gpu(fa, x)
+    r8, rsc = oracle.quantize_fp8_blockwise(x, 128)
+    np.testing.assert_array_equal(sc, rsc)
+    np.testing.assert_array_equal(x8, r8)
+    assert sc[0, 0, 0] == 1.0
+
+
+def test_quantizer_bit_exact_headline(fa):
+    """FP8 workload tensors: B=16, H=16, N=8192, d=128, 0.1% outliers x20."""
+    q, k, v = make_qkv(16, 16, 8192, 128, seed=0, outliers=True)
+    for x in (q, k, v):
+        x8, sc = _quant_gpu(fa, x)
+        r8, rsc = oracle.quantize_fp8_blockwise(x, 128)
+        np.testing.assert_array_equal(sc, rsc)
+        np.testing.assert_array_equal(x8, r8)
+
+
+def _fp8_case(fa, B, H, N, d, causal, window, seed, heads=None, rows=None):
+    q, k, v = make_qkv(B, H, N, d, seed=seed, outliers=True)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    q8, sq = fa.attn_quantize_fp8_blockwise(qd)
+    k8, sk = fa.attn_quantize_fp8_blockwise(kd)
+    v8, sv = fa.attn_quantize_fp8_blockwise(vd)
+    o, lse = fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, scale=scale, causal=causal, window=window)
+    assert fa.attn_get_device_status() == fa.ATTN_OK
+    o = o.cpu()
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    rows = rows if rows is not None else list(range(N))
+    # oracle (ii): the dequantised FP8 inputs the kernel actually consumed
+    deq = [oracle.dequantize(t8.cpu().numpy(), s.cpu().numpy(), 128)
+           for t8, s in ((q8, sq), (k8, sk), (v8, sv))]
+    o_deq, lse_deq = oracle_rows(deq[0], deq[1], deq[2], heads, rows, scale, causal, window)
+    # oracle (i): the unquantised bf16 inputs
+    o_unq, _ = oracle_rows(q, k, v, heads, rows, scale, causal, window)
+    o_g = gather(o, heads, rows)
+    lse_g = gather(lse.cpu(), heads, rows)
+    assert np.isfinite(o_g).all() and np.isfinite(lse_g).all()
+    return {
+        "vs_deq": rel_rmse(o_g, o_deq),
+        "vs_unq": rel_rmse(o_g, o_unq),
+        "oracle_deq_vs_unq": rel_rmse(o_deq, o_unq),
+        "lse_max_abs_vs_deq": float(np.abs(lse_g - lse_deq).max()),
+    }
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 300), (False, 300)])
+def test_fp8_attention_small(fa, causal, window):
+    e = _fp8_case(fa, 2, 2, 1024, 128, causal, window, seed=31)
+    assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
+    # the rest of the error against the unquantised inputs is the quantiser's
+    assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_REL_RMSE_DEQ, e
+    assert e["lse_max_abs_vs_deq"] <= 2e-2, e
+
+
+def test_fp8_attention_d256(fa):
+    e = _fp8_case(fa, 1, 2, 512, 256, True, 0, seed=32)
+    assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_attention_headline_sampled(fa, causal):
+    """FP8 workload: B=16, H=16, N=8192, d=128 with outliers; 4 heads x 96 rows."""
+    heads = sampled_heads(16, 16)
+    rows = sampled_rows(8192, 96)
+    e = _fp8_case(fa, 16, 16, 8192, 128, causal, 0, seed=0, heads=heads, rows=rows)
+    print("fp8 headline errors", e)
+    assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
+    assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_REL_RMSE_DEQ, e
