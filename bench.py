@@ -157,26 +157,28 @@ def time_steps(fn, steps, warmup, stream):
 
 
 def cpu_baseline(q, k, v, scale, budget_s=12.0):
-    """Time the float64 oracle on a bounded sample of query rows of head (0, 0)."""
+    """Time the float64 oracle, as it stands, on a bounded sample of the workload:
+    whole heads (all rows against all keys) in (b, h) order, as many as fit the budget."""
     import numpy as np
     import oracle
-    qh = q[0, 0].double().numpy()
-    kh = k[0, 0].double().numpy()
-    vh = v[0, 0].double().numpy()
-    n = qh.shape[0]
-    rows = np.arange(0, 64)
+    Bq, Hq, n, d = q.shape
+    rows = np.arange(n, dtype=np.int64)
+    heads = [(b, h) for b in range(Bq) for h in range(Hq)]
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
     t0 = time.perf_counter()
-    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows, scale, return_threads=True)
-    t_probe = time.perf_counter() - t0
-    R = int(min(n, max(64, 64 * budget_s / max(t_probe, 1e-3))))
-    rows = np.linspace(0, n - 1, R).astype(np.int64)
-    t0 = time.perf_counter()
-    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows, scale, return_threads=True)
-    dt = time.perf_counter() - t0
-    f = 4.0 * R * n * q.shape[-1]
+    _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows[:256], scale, return_threads=True)
+    per_head = (time.perf_counter() - t0) * n / 256
+    count = int(max(1, min(len(heads), budget_s / max(per_head, 1e-3))))
+    dt = 0.0
+    for (b, h) in heads[:count]:
+        qh, kh, vh = (t[b, h].double().numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        _, _, nt = oracle.attn_rows_f64(qh, kh, vh, rows, scale, return_threads=True)
+        dt += time.perf_counter() - t0
+    f = 4.0 * count * n * n * d
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": int(nt), "kind": "oracle",
-            "sample": f"{R} query rows of head (0,0) against all {n} keys, d={q.shape[-1]}, "
-                      f"non-causal, float64 ({dt:.1f} s)"}
+            "sample": f"{count} of {len(heads)} heads of the workload, every row against every "
+                      f"key (N={n}, d={d}, non-causal), float64; {dt:.1f} s of oracle time"}
 
 
 def dist_setup(args):
@@ -404,6 +406,40 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     return out
 
 
+def run_profile_case(args):
+    """A small case of one kernel for ncu: inputs still larger than L2, a few GB at most."""
+    import torch
+    import exact_attention_55_gb300 as fa
+    from exact_attention_55_gb300.inputs import make_qkv
+    fa.build.build()
+    fa.load_library()
+    torch.cuda.set_device(0)
+    b, h, n, d = 2, 16, 8192, 128       # 3 x 67 MB of Q/K/V, 64 heads' worth of work
+    q, k, v = make_qkv(b, h, n, d, seed=0, outliers=args.profile.startswith("fp8") or
+                       args.profile == "quant")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    scale = 1.0 / math.sqrt(d)
+    if args.profile in ("bf16", "bf16_causal"):
+        def run():
+            fa.attn_fwd_bf16(qd, kd, vd, scale=scale, causal=args.profile == "bf16_causal")
+    elif args.profile == "quant":
+        def run():
+            fa.attn_quantize_fp8_blockwise(qd)
+    else:
+        qs = [fa.attn_quantize_fp8_blockwise(t) for t in (qd, kd, vd)]
+
+        def run():
+            fa.attn_fwd_fp8(qs[0][0], qs[1][0], qs[2][0], qs[0][1], qs[1][1], qs[2][1],
+                            scale=scale, causal=args.profile == "fp8_causal")
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    status = fa.attn_get_device_status()
+    print(json.dumps({"profile_case": args.profile, "shape": [b, h, n, d], "status": status}))
+    if status != fa.ATTN_OK:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -411,7 +447,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
+    ap.add_argument("--profile", default=None,
+                    choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant"],
+                    help="run a small case of one kernel (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup(args)

@@ -248,129 +248,138 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
         }
     } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs this loop in lock-step with warp-uniform values; one
+        // elected lane issues each tcgen05 instruction.  Descriptors are built once
+        // and every MMA only adds a compile-time offset, so issue keeps pace with
+        // the tensor core.
         if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
-        if (lane == 0) {
-            constexpr uint32_t fmt = F8 ? 0u : 1u;
-            constexpr uint32_t idesc_s = idesc_f32acc(fmt, 0, C::BM, C::BN);
-            constexpr uint32_t idesc_o = idesc_f32acc(fmt, 1, C::BM, D);
-            const uint32_t q_base = smem_u32(q_smem);
-            const uint32_t kv_base = smem_u32(kv_smem);
-            uint32_t ring = 0, uc = 0;
-            uint32_t p_phase = 0;  // bit b: parity of the next p_full[b] completion
-            bool ok = true;
+        constexpr uint32_t fmt = F8 ? 0u : 1u;
+        constexpr uint32_t idesc_s = idesc_f32acc(fmt, 0, C::BM, C::BN);
+        constexpr uint32_t idesc_o = idesc_f32acc(fmt, 1, C::BM, D);
+        const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem), 16, 1024);
+        const uint64_t k_desc0 = sdesc_sw128(smem_u32(kv_smem), 16, 1024);
+        const uint64_t v_desc0 = sdesc_sw128(smem_u32(kv_smem), C::CB_KV_BYTES, 1024);
+        uint32_t ring = 0, uc = 0;
+        uint32_t p_phase = 0;  // bit b: parity of the next p_full[b] completion
+        bool ok = true;
 
-            auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-                if (!ok) return false;
-                if (!mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns)) ok = false;
-                return ok;
-            };
-            // S[sb] = Q_i K^T with K in ring slot `slot`
-            auto issue_s = [&](int i, int sb, uint32_t slot) {
-                const uint32_t a0 = q_base + i * C::Q_BYTES;
-                const uint32_t b0 = kv_base + slot * C::KV_BYTES;
-                const uint32_t d_t = tmem + C::S_COL0 + sb * C::BN;
+        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
+            r = __all_sync(0xffffffffu, r);
+            if (!r) ok = false;
+            return r;
+        };
+        auto commit = [&](uint64_t* bar) { mma_commit_warp(smem_u32(bar)); };
+        // S[sb] = Q_i K^T with K in ring slot `slot`
+        auto issue_s = [&](int i, int sb, uint32_t slot) {
+            const uint64_t qa = q_desc0 + (uint64_t)((i * C::Q_BYTES) >> 4);
+            const uint64_t kb = k_desc0 + (uint64_t)((slot * C::KV_BYTES) >> 4);
+            const uint32_t d_t = tmem + C::S_COL0 + sb * C::BN;
 #pragma unroll
-                for (int kk = 0; kk < D / C::K_STEP; ++kk) {
-                    const int byte = kk * C::K_STEP * C::EB;  // offset along the row
-                    const uint32_t off_a = (byte / 128) * C::CB_Q_BYTES + (byte % 128);
-                    const uint32_t off_b = (byte / 128) * C::CB_KV_BYTES + (byte % 128);
-                    mma_ss<F8>(d_t, sdesc_sw128(a0 + off_a, 16, 1024),
-                               sdesc_sw128(b0 + off_b, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
-            };
-            // O_i (+)= P[sb] V with V in ring slot `slot` (V is MN-major: d contiguous)
-            auto issue_pv = [&](int i, int sb, uint32_t slot, bool accumulate) {
-                const uint32_t b0 = kv_base + slot * C::KV_BYTES;
-                const uint32_t d_t = tmem + C::O_COL0 + i * D;
-                const uint32_t a_t = tmem + C::S_COL0 + sb * C::BN;
+            for (int kk = 0; kk < D / C::K_STEP; ++kk) {
+                constexpr int step_bytes = C::K_STEP * C::EB;  // along the row
+                const int byte = kk * step_bytes;
+                const uint32_t off_a = ((byte / 128) * C::CB_Q_BYTES + (byte % 128)) >> 4;
+                const uint32_t off_b = ((byte / 128) * C::CB_KV_BYTES + (byte % 128)) >> 4;
+                mma_ss_warp<F8>(d_t, qa + off_a, kb + off_b, idesc_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // O_i (+)= P[sb] V with V in ring slot `slot` (V is MN-major: d contiguous)
+        auto issue_pv = [&](int i, int sb, uint32_t slot, bool accumulate) {
+            const uint64_t vb = v_desc0 + (uint64_t)((slot * C::KV_BYTES) >> 4);
+            const uint32_t d_t = tmem + C::O_COL0 + i * D;
+            const uint32_t a_t = tmem + C::S_COL0 + sb * C::BN;
+            const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < C::BN / C::K_STEP; ++kk) {
-                    const uint32_t off_b = kk * C::K_STEP * 128;  // K_STEP key rows of 128 B
-                    mma_ts<F8>(d_t, a_t + kk * (C::K_STEP * C::EB / 4),
-                               sdesc_sw128(b0 + off_b, C::CB_KV_BYTES, 1024), idesc_o,
-                               (accumulate || kk > 0) ? 1u : 0u);
-                }
-            };
+            for (int kk = 0; kk < C::BN / C::K_STEP; ++kk) {
+                const uint32_t off_b = (kk * C::K_STEP * 128) >> 4;  // K_STEP key rows of 128 B
+                mma_ts_warp<F8>(d_t, a_t + kk * (C::K_STEP * C::EB / 4), vb + off_b, idesc_o,
+                                kk > 0 ? 1u : acc0);
+            }
+        };
 
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-                const Unit w = unit_of<C>(u, p);
-                for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
-                tc_fence_after_sync();
-                // step 0: S(0) for every Q tile
-                {
-                    const uint32_t slot = ring % C::NSLOT;
-                    if (!wait(&bars->kv_full[slot], (ring / C::NSLOT) & 1)) break;
-                    for (int i = 0; i < C::NQ; ++i) {
-                        issue_s(i, i, slot);
-                        mma_commit(smem_u32(&bars->s_full[i]));
-                        if (w.n == 1) mma_commit(smem_u32(&bars->q_empty[i]));
-                    }
-                    mma_commit(smem_u32(&bars->kv_empty[slot]));
-                    ++ring;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
+            const Unit w = unit_of<C>(u, p);
+#pragma unroll
+            for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
+            tc_fence_after_sync();
+            // step 0: S(0) for every Q tile
+            {
+                const uint32_t slot = ring % C::NSLOT;
+                if (!wait(&bars->kv_full[slot], (ring / C::NSLOT) & 1)) break;
+#pragma unroll
+                for (int i = 0; i < C::NQ; ++i) {
+                    issue_s(i, i, slot);
+                    commit(&bars->s_full[i]);
+                    if (w.n == 1) commit(&bars->q_empty[i]);
                 }
-                for (int jj = 1; jj < w.n && ok; ++jj) {
-                    const uint32_t slot_v = ring % C::NSLOT;         // V_{jj-1}
-                    const uint32_t slot_k = (ring + 1) % C::NSLOT;   // K_jj
-                    const uint32_t par_v = (ring / C::NSLOT) & 1;
-                    const uint32_t par_k = ((ring + 1) / C::NSLOT) & 1;
-                    if constexpr (C::NQ == 2) {
-                        if (!wait(&bars->kv_full[slot_v], par_v)) break;
-                        for (int i = 0; i < 2; ++i) {
-                            if (!wait(&bars->p_full[i], (p_phase >> i) & 1)) break;
-                            p_phase ^= 1u << i;
-                            if (jj == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
-                            tc_fence_after_sync();
-                            issue_pv(i, i, slot_v, jj > 1);
-                            mma_commit(smem_u32(&bars->pv_done[i]));
-                            if (i == 0 && !wait(&bars->kv_full[slot_k], par_k)) break;
-                            issue_s(i, i, slot_k);
-                            mma_commit(smem_u32(&bars->s_full[i]));
-                            if (jj == w.n - 1) mma_commit(smem_u32(&bars->q_empty[i]));
-                        }
-                    } else {
-                        const int sb = jj & 1, sp = (jj - 1) & 1;
-                        if (!wait(&bars->kv_full[slot_k], par_k)) break;
-                        issue_s(0, sb, slot_k);
-                        mma_commit(smem_u32(&bars->s_full[sb]));
-                        if (jj == w.n - 1) mma_commit(smem_u32(&bars->q_empty[0]));
-                        if (!wait(&bars->kv_full[slot_v], par_v)) break;
-                        if (!wait(&bars->p_full[sp], (p_phase >> sp) & 1)) break;
-                        p_phase ^= 1u << sp;
-                        if (jj == 1 && !wait(&bars->o_empty[0], (uc & 1) ^ 1)) break;
+                commit(&bars->kv_empty[slot]);
+                ++ring;
+            }
+            for (int jj = 1; jj < w.n && ok; ++jj) {
+                const uint32_t slot_v = ring % C::NSLOT;         // V_{jj-1}
+                const uint32_t slot_k = (ring + 1) % C::NSLOT;   // K_jj
+                const uint32_t par_v = (ring / C::NSLOT) & 1;
+                const uint32_t par_k = ((ring + 1) / C::NSLOT) & 1;
+                if constexpr (C::NQ == 2) {
+                    if (!wait(&bars->kv_full[slot_v], par_v)) break;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (!wait(&bars->p_full[i], (p_phase >> i) & 1)) break;
+                        p_phase ^= 1u << i;
+                        if (jj == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
                         tc_fence_after_sync();
-                        issue_pv(0, sp, slot_v, jj > 1);
-                        mma_commit(smem_u32(&bars->pv_done[0]));
+                        issue_pv(i, i, slot_v, jj > 1);
+                        commit(&bars->pv_done[i]);
+                        if (i == 0 && !wait(&bars->kv_full[slot_k], par_k)) break;
+                        issue_s(i, i, slot_k);
+                        commit(&bars->s_full[i]);
+                        if (jj == w.n - 1) commit(&bars->q_empty[i]);
                     }
-                    if (!ok) break;
-                    mma_commit(smem_u32(&bars->kv_empty[slot_v]));
-                    mma_commit(smem_u32(&bars->kv_empty[slot_k]));
-                    ring += 2;
+                } else {
+                    const int sb = jj & 1, sp = (jj - 1) & 1;
+                    if (!wait(&bars->kv_full[slot_k], par_k)) break;
+                    issue_s(0, sb, slot_k);
+                    commit(&bars->s_full[sb]);
+                    if (jj == w.n - 1) commit(&bars->q_empty[0]);
+                    if (!wait(&bars->kv_full[slot_v], par_v)) break;
+                    if (!wait(&bars->p_full[sp], (p_phase >> sp) & 1)) break;
+                    p_phase ^= 1u << sp;
+                    if (jj == 1 && !wait(&bars->o_empty[0], (uc & 1) ^ 1)) break;
+                    tc_fence_after_sync();
+                    issue_pv(0, sp, slot_v, jj > 1);
+                    commit(&bars->pv_done[0]);
                 }
                 if (!ok) break;
-                // tail: P(n-1) V_{n-1}
-                {
-                    const uint32_t slot_v = ring % C::NSLOT;
-                    if (!wait(&bars->kv_full[slot_v], (ring / C::NSLOT) & 1)) break;
-                    const int sp = (C::NQ == 2) ? 0 : ((w.n - 1) & 1);
-                    for (int i = 0; i < C::NQ; ++i) {
-                        const int sb = (C::NQ == 2) ? i : sp;
-                        if (!wait(&bars->p_full[sb], (p_phase >> sb) & 1)) break;
-                        p_phase ^= 1u << sb;
-                        if (w.n == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
-                        tc_fence_after_sync();
-                        issue_pv(i, sb, slot_v, w.n > 1);
-                        mma_commit(smem_u32(&bars->pv_done[i]));
-                    }
-                    if (!ok) break;
-                    mma_commit(smem_u32(&bars->kv_empty[slot_v]));
-                    ++ring;
-                }
+                commit(&bars->kv_empty[slot_v]);
+                commit(&bars->kv_empty[slot_k]);
+                ring += 2;
             }
-            if (!ok) raise_timeout(p, bars);
-            // Drain: every MMA this thread issued has finished before TMEM is freed.
-            mma_commit(smem_u32(&bars->drain));
-            mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+            if (!ok) break;
+            // tail: P(n-1) V_{n-1}
+            {
+                const uint32_t slot_v = ring % C::NSLOT;
+                if (!wait(&bars->kv_full[slot_v], (ring / C::NSLOT) & 1)) break;
+                const int sp = (C::NQ == 2) ? 0 : ((w.n - 1) & 1);
+#pragma unroll
+                for (int i = 0; i < C::NQ; ++i) {
+                    const int sb = (C::NQ == 2) ? i : sp;
+                    if (!wait(&bars->p_full[sb], (p_phase >> sb) & 1)) break;
+                    p_phase ^= 1u << sb;
+                    if (w.n == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
+                    tc_fence_after_sync();
+                    issue_pv(i, sb, slot_v, w.n > 1);
+                    commit(&bars->pv_done[i]);
+                }
+                if (!ok) break;
+                commit(&bars->kv_empty[slot_v]);
+                ++ring;
+            }
         }
+        if (!ok && lane == 0) raise_timeout(p, bars);
+        // Drain: every MMA this warp issued has finished before TMEM is freed.
+        commit(&bars->drain);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
         __syncwarp();
     } else if (warp < C::NUM_SOFTMAX_WARPS) {
         // ------------------------------------------------------------ softmax groups
@@ -425,16 +434,16 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 s_phase ^= 1u << sb;
                 tc_fence_after_sync();
 
-                float s[C::BN];
+                // S row -> registers: issue every load, then one wait
+                uint32_t sr[C::BN];
                 const uint32_t s_addr = tmem + lane_addr + C::S_COL0 + sb * C::BN;
 #pragma unroll
-                for (int ch = 0; ch < C::BN / 32; ++ch) {
-                    uint32_t r[32];
-                    tmem_ld32(s_addr + ch * 32, r);
-                    tmem_wait_ld(r);
+                for (int ch = 0; ch < C::BN / 32; ++ch) tmem_ld32p(s_addr + ch * 32, sr + ch * 32);
+                tmem_wait_ld_only();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(r[e]);
-                }
+                for (int ch = 0; ch < C::BN / 32; ++ch) reg_fence32(sr + ch * 32);
+                float* s = reinterpret_cast<float*>(sr);
+
                 // mask only on tiles that cross a boundary of some row's allowed set
                 const bool edge = (c0 + C::BN > p.N) || (p.causal && c0 + C::BN - 1 > a) ||
                                   (p.window > 0 &&
@@ -447,82 +456,104 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                         if (j < jlo || j > jhi) s[e] = NEG_INF;
                     }
                 }
-                float tmax = s[0];
+                // row max: 8 independent chains of 3-input maxima, then a small tree
+                float mx[8];
 #pragma unroll
-                for (int e = 1; e < C::BN; ++e) tmax = fmaxf(tmax, s[e]);
+                for (int k = 0; k < 8; ++k) {
+                    constexpr int PER = C::BN / 8;
+                    float m = s[k];
+#pragma unroll
+                    for (int u2 = 1; u2 + 1 < PER; u2 += 2) m = fmax3(m, s[k + 8 * u2], s[k + 8 * u2 + 8]);
+                    if constexpr (PER % 2 == 0) m = fmaxf(m, s[k + 8 * (PER - 1)]);
+                    mx[k] = m;
+                }
+                const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                         fmaxf(mx[6], mx[7]));
                 const float m_cand = tmax * c;
                 const float m_new = fmaxf(m_used, m_cand);
                 // bf16: move the max only when it grew by more than TAU; fp8: always
                 const bool resc = F8 ? (m_new > m_used) : (m_cand > m_used + C::TAU);
                 const float alpha = resc ? ex2(m_used - m_new) : 1.0f;  // ex2(-inf) = 0
-                bool any_resc = false;
-                if (jj > 0) {
-                    any_resc = F8 ? true : __any_sync(0xffffffffu, resc);
-                    if (any_resc) {
-                        // O must hold P(jj-1) V before it is rescaled
-                        if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
-                        pv_phase ^= 1u << grp;
-                        tc_fence_after_sync();
-                        const float f = alpha * dv_ratio;
-                        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
-#pragma unroll
-                        for (int ch = 0; ch < D / 32; ++ch) {
-                            uint32_t r[32];
-                            tmem_ld32(o_addr + ch * 32, r);
-                            tmem_wait_ld(r);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                            tmem_st32(o_addr + ch * 32, r);
-                        }
-                    }
-                }
                 if (resc) {
                     l *= alpha;
                     m_used = m_new;
                 }
+                // P = 2^(s*c - m) (fp8: times 2^P8_SHIFT, folded into the exponent)
                 const float mb = (m_used == NEG_INF) ? 0.0f : m_used;
-                float rowsum = 0.0f;
+                const float2 c2 = make_float2(c, c);
+                const float bias = F8 ? float(C::P8_SHIFT) - mb : -mb;
+                const float2 b2 = make_float2(bias, bias);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 const uint32_t p_addr = tmem + lane_addr + C::S_COL0 + sb * C::BN;
                 if constexpr (!F8) {
 #pragma unroll
                     for (int ch = 0; ch < C::BN / 64; ++ch) {
-                        uint32_t r[32];
+                        uint32_t pk[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const float p0 = ex2(fmaf(s[ch * 64 + 2 * e], c, -mb));
-                            const float p1 = ex2(fmaf(s[ch * 64 + 2 * e + 1], c, -mb));
-                            rowsum += p0 + p1;
-                            r[e] = pack_bf16x2(p0, p1);
+                            const int i0 = ch * 64 + 2 * e;
+                            const float2 x = __ffma2_rn(make_float2(s[i0], s[i0 + 1]), c2, b2);
+                            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                            acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+                            pk[e] = pack_bf16x2(pp.x, pp.y);
                         }
-                        tmem_st32(p_addr + ch * 32, r);
+                        tmem_st32p(p_addr + ch * 32, pk);
                     }
                 } else {
 #pragma unroll
                     for (int ch = 0; ch < C::BN / 128; ++ch) {
-                        uint32_t r[32];
+                        uint32_t pk[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
-                            const float* sp = &s[ch * 128 + 4 * e];
-                            const float p0 = ex2(fmaf(sp[0], c, -mb));
-                            const float p1 = ex2(fmaf(sp[1], c, -mb));
-                            const float p2 = ex2(fmaf(sp[2], c, -mb));
-                            const float p3 = ex2(fmaf(sp[3], c, -mb));
-                            rowsum += (p0 + p1) + (p2 + p3);
-                            constexpr float ps = float(1u << C::P8_SHIFT);
-                            const uint32_t lo = pack_e4m3x2(p0 * ps, p1 * ps);
-                            const uint32_t hi = pack_e4m3x2(p2 * ps, p3 * ps);
-                            r[e] = lo | (hi << 16);
+                            const int i0 = ch * 128 + 4 * e;
+                            const float2 x0 = __ffma2_rn(make_float2(s[i0], s[i0 + 1]), c2, b2);
+                            const float2 x1 = __ffma2_rn(make_float2(s[i0 + 2], s[i0 + 3]), c2, b2);
+                            const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                            const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                            acc[(2 * e) & 3] = __fadd2_rn(acc[(2 * e) & 3], p0);
+                            acc[(2 * e + 1) & 3] = __fadd2_rn(acc[(2 * e + 1) & 3], p1);
+                            pk[e] = (uint32_t)pack_e4m3x2(p0.x, p0.y) |
+                                    ((uint32_t)pack_e4m3x2(p1.x, p1.y) << 16);
                         }
-                        tmem_st32(p_addr + ch * 32, r);
+                        tmem_st32p(p_addr + ch * 32, pk);
                     }
                 }
+                const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+                const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+                float rowsum = (a01.x + a01.y) + (a23.x + a23.y);
+                if constexpr (F8) rowsum *= 1.0f / float(1u << C::P8_SHIFT);
                 l += rowsum;
-                tmem_wait_st();
-                if (jj > 0 && !any_resc) {
+
+                if (jj > 0) {
+                    // O must hold P(jj-1) V before it is rescaled, and PV(jj) must not
+                    // start before this group has seen PV(jj-1) complete.
                     if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
                     pv_phase ^= 1u << grp;
+                    const bool any_resc = F8 ? true : __any_sync(0xffffffffu, resc);
+                    if (any_resc) {
+                        tc_fence_after_sync();
+                        const float f = alpha * dv_ratio;
+                        const float2 f2 = make_float2(f, f);
+                        const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
+#pragma unroll
+                        for (int ch = 0; ch < D / 32; ++ch) {
+                            uint32_t r[32];
+                            tmem_ld32p(o_addr + ch * 32, r);
+                            tmem_wait_ld_only();
+                            reg_fence32(r);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 v2 = __fmul2_rn(
+                                    make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), f2);
+                                r[2 * e] = __float_as_uint(v2.x);
+                                r[2 * e + 1] = __float_as_uint(v2.y);
+                            }
+                            tmem_st32p(o_addr + ch * 32, r);
+                        }
+                    }
                 }
+                tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[sb]));

@@ -3,7 +3,12 @@ and the error measures with the tolerances the tests assert.
 
 Tolerances (fixed by the specification of this path):
   bf16:  max |dO| <= 1.5e-2, mean |dO| <= 1e-3, max |dLSE| <= 1e-3 (inputs N(0,1))
-  fp8:   RMSE(dO)/RMS(O) <= 1e-2 against the oracle on the dequantised FP8 inputs
+  fp8:   RMSE(dO)/RMS(O) <= 1e-2 against the oracle on the dequantised FP8 inputs,
+         on the FP8 workload's distribution (N(0,1) with 0.1% x20 outliers, d = 128)
+  fp8, other shapes and distributions: the bound set by rounding P to E4M3.  RNE
+         to 3 mantissa bits leaves a relative error of at most 2^-4 per element; a
+         weighted average of such independent errors has a relative RMS of at most
+         2^-4 / sqrt(3) ~= 0.036 (error uniform over +-2^-4).
 """
 from __future__ import annotations
 
@@ -17,6 +22,7 @@ BF16_MEAN_ABS = 1e-3
 LSE_MAX_ABS = 1e-3
 FP8_REL_RMSE_DEQ = 1e-2
 FP8_REL_RMSE_UNQ = 4e-2
+FP8_P_ROUNDING_BOUND = 2.0 ** -4 / 3.0 ** 0.5
 
 
 def oracle_rows(q, k, v, heads, rows, scale, causal, window):

@@ -8,7 +8,8 @@ import torch
 
 import oracle
 from exact_attention_55_gb300.inputs import make_qkv, sampled_heads, sampled_rows
-from tests.attn_check import FP8_REL_RMSE_DEQ, gather, oracle_rows, rel_rmse
+from tests.attn_check import (FP8_P_ROUNDING_BOUND, FP8_REL_RMSE_DEQ, gather, oracle_rows,
+                              rel_rmse)
 from tests.conftest import require_gpu
 
 pytestmark = pytest.mark.gpu
@@ -58,8 +59,8 @@ def test_quantizer_bit_exact_headline(fa):
         np.testing.assert_array_equal(x8, r8)
 
 
-def _fp8_case(fa, B, H, N, d, causal, window, seed, heads=None, rows=None):
-    q, k, v = make_qkv(B, H, N, d, seed=seed, outliers=True)
+def _fp8_case(fa, B, H, N, d, causal, window, seed, heads=None, rows=None, outliers=True):
+    q, k, v = make_qkv(B, H, N, d, seed=seed, outliers=outliers)
     scale = 1.0 / math.sqrt(d)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     q8, sq = fa.attn_quantize_fp8_blockwise(qd)
@@ -96,9 +97,36 @@ def test_fp8_attention_small(fa, causal, window):
     assert e["lse_max_abs_vs_deq"] <= 2e-2, e
 
 
-def test_fp8_attention_d256(fa):
-    e = _fp8_case(fa, 1, 2, 512, 256, True, 0, seed=32)
-    assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_attention_d256(fa, causal):
+    e = _fp8_case(fa, 1, 2, 512, 256, causal, 0, seed=32)
+    assert e["vs_deq"] <= FP8_P_ROUNDING_BOUND, e
+    assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_P_ROUNDING_BOUND, e
+
+
+def test_fp8_attention_without_outliers(fa):
+    """Spread attention (no outliers): P's E4M3 rounding dominates the error."""
+    e = _fp8_case(fa, 1, 4, 1024, 128, False, 0, seed=33, outliers=False)
+    assert e["vs_deq"] <= FP8_P_ROUNDING_BOUND, e
+
+
+def test_fp8_closed_form_zero_query(fa):
+    """Q = 0: every allowed key gets the same weight, so O is the mean of the
+    dequantised V rows and P = 1 is exact in E4M3."""
+    B, H, N, d = 1, 2, 512, 128
+    _, k, v = make_qkv(B, H, N, d, seed=34, outliers=True)
+    q = torch.zeros_like(k)
+    qs = [fa.attn_quantize_fp8_blockwise(t.cuda()) for t in (q, k, v)]
+    o, lse = fa.attn_fwd_fp8(qs[0][0], qs[1][0], qs[2][0], qs[0][1], qs[1][1], qs[2][1],
+                             scale=0.1, causal=True)
+    assert fa.attn_get_device_status() == fa.ATTN_OK
+    vdeq = oracle.dequantize(qs[2][0].cpu().numpy(), qs[2][1].cpu().numpy(), 128)
+    o = o.cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    for i in (0, 1, 127, 128, 300, 511):
+        ref = vdeq[:, :, :i + 1].mean(axis=2)
+        assert np.abs(o[:, :, i] - ref).max() <= 1e-2 * max(1.0, np.abs(ref).max())
+        assert np.abs(lse[:, :, i] - math.log(i + 1)).max() <= 1e-5
 
 
 @pytest.mark.parametrize("causal", [False, True])
