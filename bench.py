@@ -54,10 +54,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "profiling-recipe fallback"
 
 
-def kernel_source_hash():
+ATTN_KERNEL_FILES = ("attn_fwd.cuh", "attn_fwd_inst.cu", "attn_params.h", "ptx.cuh")
+
+
+def kernel_source_hash(files=ATTN_KERNEL_FILES):
+    """Hash of the sources that define the attention kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_55_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -113,8 +113,8 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.BH = BH;
     p.N = N;
     p.num_qblk = (N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
-    const long long units = (long long)BH * p.num_qblk;
-    if (units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    const long long units = (long long)BH * ((p.num_qblk + 1) / 2);
+    if (2 * units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     p.causal = causal ? 1 : 0;
     p.window = window > 0 ? window : 0;
@@ -198,6 +198,7 @@ extern "C" attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, fl
     p.x = x;
     p.x8 = static_cast<uint8_t*>(x8);
     p.scales = scales;
+    p.status = dev->status;
     p.BH = (int)BH;
     p.N = N;
     p.d = d;

@@ -108,17 +108,24 @@ struct Unit {
     int n;       // key tiles visited
 };
 
-// Work unit u -> (head, query block, key-tile range).  Units of one head are
-// adjacent so concurrently running CTAs share that head's K/V in L2; with a
-// causal or banded mask the query blocks of a head run last-first so the
-// longest units start first.
+// Work decomposition.  A work unit is (head, query block of NQ*128 rows).  The
+// query blocks of a head are handed out in complementary pairs (nq-1-k, k): under
+// a causal mask the two halves' key ranges add up to the same count for every k,
+// so giving pairs to CTAs round-robin balances the persistent grid without a
+// runtime scheduler ("dynamic load balancing" is what the pages ask for; here the
+// balance is built into the order).  Pairs of one head are adjacent, so CTAs that
+// run at the same time share that head's K/V in L2.  Sub-unit s is half (s & 1)
+// of pair s >> 1, the heavy half first; a CTA walks 2c, 2c+1, 2c+2G, 2c+2G+1, ...
+// Returns false for the empty second half of the middle pair when nq is odd.
 template <class C>
-__device__ __forceinline__ Unit unit_of(int u, const FwdParams& p)
+__device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w)
 {
-    Unit w;
-    w.bh = u / p.num_qblk;
-    int qb = u % p.num_qblk;
-    if (p.causal || p.window > 0) qb = p.num_qblk - 1 - qb;
+    const int npair = (p.num_qblk + 1) >> 1;
+    const int pair = s >> 1;
+    const int k = pair % npair;
+    w.bh = pair / npair;
+    const int qb = (s & 1) ? k : p.num_qblk - 1 - k;
+    if ((s & 1) && qb == p.num_qblk - 1 - k) return false;
     w.q0 = qb * (C::NQ * C::BM);
     const int r_last = min(p.N, w.q0 + C::NQ * C::BM) - 1;
     int lo = 0, hi = p.N;  // keys [lo, hi) that some row of the unit may use
@@ -127,8 +134,10 @@ __device__ __forceinline__ Unit unit_of(int u, const FwdParams& p)
     else if (p.window > 0) hi = min(p.N, r_last + p.window + 1);
     w.t0 = lo / C::BN;
     w.n = (hi + C::BN - 1) / C::BN - w.t0;
-    return w;
+    return true;
 }
+
+__device__ __forceinline__ int next_sub(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
 
 __device__ __forceinline__ void raise_timeout(const FwdParams& p, FwdBars* bars)
 {
@@ -192,8 +201,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             uint32_t ring = 0, uc = 0;
             uint32_t q_armed[2] = {0, 0};
             bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-                const Unit w = unit_of<C>(u, p);
+            for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+                Unit w;
+                if (!unit_of<C>(su, p, w)) continue;
                 for (int i = 0; i < C::NQ && ok; ++i) {
                     const uint32_t fb = smem_u32(&bars->q_full[i]);
                     if (!mbar_wait(smem_u32(&bars->q_empty[i]), (uc & 1) ^ 1, abort_flag,
@@ -231,6 +241,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                         ++ring;
                     }
                 }
+                ++uc;
             }
             if (!ok) {
                 raise_timeout(p, bars);
@@ -298,8 +309,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             }
         };
 
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-            const Unit w = unit_of<C>(u, p);
+        for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+            Unit w;
+            if (!unit_of<C>(su, p, w)) continue;
 #pragma unroll
             for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
             tc_fence_after_sync();
@@ -375,6 +387,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 commit(&bars->kv_empty[slot_v]);
                 ++ring;
             }
+            ++uc;
         }
         if (!ok && lane == 0) raise_timeout(p, bars);
         // Drain: every MMA this warp issued has finished before TMEM is freed.
@@ -400,8 +413,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             return r;
         };
 
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++uc) {
-            const Unit w = unit_of<C>(u, p);
+        for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+            Unit w;
+            if (!unit_of<C>(su, p, w)) continue;
             const int a = w.q0 + grp * C::BM;    // first row of this Q tile
             const int row = a + row_in_tile;     // this thread's query row
             // keys allowed for this row: [jlo, jhi]
@@ -592,6 +606,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : NEG_INF;
                 p.lse[(size_t)w.bh * p.N + row] = lse2 * 0.69314718055994531f;
             }
+            ++uc;
         }
         if (!ok) raise_timeout(p, bars);
     } else {

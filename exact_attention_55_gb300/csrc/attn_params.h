@@ -21,7 +21,7 @@ struct FwdParams {
     int BH;               // batch * heads
     int N;                // sequence length (queries = keys)
     int num_qblk;         // query blocks per head (NQ * 128 rows each)
-    int num_units;        // BH * num_qblk
+    int num_units;        // BH * ceil(num_qblk / 2): pairs of query blocks
     int causal;           // 1: key j allowed only for j <= i
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
@@ -32,6 +32,7 @@ struct QuantParams {
     const void* x;        // bf16 [BH, N, d]
     uint8_t* x8;          // e4m3 [BH, N, d]
     float* scales;        // fp32 [BH, ceil(N/128)]
+    int* status;          // device status word (timeouts)
     int BH, N, d;
     int nblk;             // ceil(N / 128)
 };

@@ -7,9 +7,22 @@
 //
 // For each (head, block of 128 rows, all d columns):
 //   amax  = max |x|;  scale = amax / 448 (IEEE fp32 division), or 1 when amax == 0
-//   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 division, one rounding to E4M3)
-// The kernel is HBM-bound: it reads each bf16 element once (kept in registers for
-// the second pass) and writes one byte per element plus one float per block.
+//   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 quotient, one rounding to E4M3)
+//
+// HBM-bound design: one persistent CTA per SM streams whole blocks (one
+// contiguous run of rows * d * 2 bytes) into a 3-stage shared-memory ring with
+// cp.async.bulk, so several blocks are in flight per SM while the threads reduce
+// and convert the current one.  Each element is read from HBM once and written
+// as one byte.
+//
+// The quotient x / scale is formed from the correctly rounded reciprocal
+// y = RN(1/scale) with one residual correction, q = RN(x*y), r = x - scale*q
+// (exact with an FMA), q' = RN(q + r*y) -- Markstein's final division step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990), which gives the correctly
+// rounded quotient without a per-element divide.  The GPU tests compare the
+// result bit for bit with the oracle's IEEE division over every pair of bf16
+// mantissas.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -18,40 +31,88 @@
 
 namespace gb300 {
 
-constexpr int kQuantThreads = 256;
+constexpr int kQuantThreads = 512;
 constexpr int kQuantRows = 128;
-// 16-element groups per thread: 128 rows * 256 cols / 16 / 256 threads
-constexpr int kQuantGroupsPerThread = 8;
+constexpr int kQuantStages = 3;
+constexpr int kQuantStageBytes = kQuantRows * 256 * 2;  // a block of up to d = 256 bf16 columns
+constexpr int kQuantSmemBytes = 128 + kQuantStages * kQuantStageBytes + 64;
+constexpr unsigned long long kQuantTimeoutNs = 4000000000ull;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__global__ void __launch_bounds__(kQuantThreads) quant_fp8_kernel(const QuantParams p)
+// RN(x / s) for s > 0 finite and a normal quotient, from y = RN(1/s).
+__device__ __forceinline__ float div_by_scale(float x, float s, float y)
 {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    return (r == 0.0f) ? q : __fmaf_rn(r, y, q);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const QuantParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                               ~uintptr_t(127));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * kQuantStageBytes);
     __shared__ float warp_max[kQuantThreads / 32];
+    __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = p.BH * p.nblk;
-    for (int blk = blockIdx.x; blk < total; blk += gridDim.x) {
-        const int bh = blk / p.nblk, b = blk % p.nblk;
-        const int r0 = b * kQuantRows;
-        const int rows = min(kQuantRows, p.N - r0);
-        const size_t base = ((size_t)bh * p.N + r0) * p.d;  // element offset of the block
-        const int ngroups = rows * p.d / 16;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(p.x) + base);
-        uint4 raw[kQuantGroupsPerThread][2];
-        float amax = 0.0f;
-#pragma unroll
-        for (int v = 0; v < kQuantGroupsPerThread; ++v) {
-            const int g = threadIdx.x + v * kQuantThreads;
-            if (g < ngroups) {
-                raw[v][0] = __ldcs(src + 2 * g);
-                raw[v][1] = __ldcs(src + 2 * g + 1);
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(raw[v]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
+
+    auto block_rows = [&](int blk) { return min(kQuantRows, p.N - (blk % p.nblk) * kQuantRows); };
+    auto block_base = [&](int blk) {  // element offset of the block
+        return ((size_t)(blk / p.nblk) * p.N + (size_t)(blk % p.nblk) * kQuantRows) * p.d;
+    };
+    auto issue = [&](int blk, int stage) {
+        const uint32_t bytes = (uint32_t)block_rows(blk) * p.d * 2;
+        const uint32_t bar = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(smem_u32(smem + stage * kQuantStageBytes), x + block_base(blk), bytes, bar);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQuantStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        for (int s = 0; s < kQuantStages; ++s) {
+            const int blk = blockIdx.x + s * gridDim.x;
+            if (blk < total) issue(blk, s);
+        }
+    }
+    __syncthreads();
+
+    int it = 0;
+    for (int blk = blockIdx.x; blk < total; blk += gridDim.x, ++it) {
+        const int stage = it % kQuantStages;
+        const uint32_t parity = (it / kQuantStages) & 1;
+        bool ok = mbar_wait(smem_u32(&full[stage]), parity, &abort_flag, kQuantTimeoutNs);
+        if (!__syncthreads_and(ok)) {
+            if (threadIdx.x == 0) {
+                abort_flag = 1;
+                atomicExch(p.status, kStatusTimeout);
             }
+            break;
+        }
+        const uint8_t* st = smem + stage * kQuantStageBytes;
+        const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
+        float amax = 0.0f;
+        for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
         }
 #pragma unroll
         for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
@@ -61,36 +122,55 @@ __global__ void __launch_bounds__(kQuantThreads) quant_fp8_kernel(const QuantPar
 #pragma unroll
         for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
         const float scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        const float y = __frcp_rn(scale);
 
-        uint4* dst = reinterpret_cast<uint4*>(p.x8 + base);
+        uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
+        for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[2];
 #pragma unroll
-        for (int v = 0; v < kQuantGroupsPerThread; ++v) {
-            const int g = threadIdx.x + v * kQuantThreads;
-            if (g < ngroups) {
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(raw[v]);
-                uint32_t out[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(w[2 * e]), scale),
-                                                    __fdiv_rn(bf16_hi(w[2 * e]), scale));
-                    const uint32_t hi = pack_e4m3x2(__fdiv_rn(bf16_lo(w[2 * e + 1]), scale),
-                                                    __fdiv_rn(bf16_hi(w[2 * e + 1]), scale));
-                    out[e] = lo | (hi << 16);
-                }
-                __stcs(dst + g, make_uint4(out[0], out[1], out[2], out[3]));
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t lo = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
+                                                div_by_scale(bf16_hi(w[2 * e]), scale, y));
+                const uint32_t hi = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
+                                                div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
+                out[e] = lo | (hi << 16);
             }
+            __stcs(dst + g, make_uint2(out[0], out[1]));
         }
         if (threadIdx.x == 0) p.scales[blk] = scale;
-        __syncthreads();  // warp_max is reused by the next block
+        // every thread is done with this stage (and with warp_max) before it is refilled
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const int next = blk + kQuantStages * gridDim.x;
+            if (next < total) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, stage);
+            }
+        }
+    }
+    // Let every copy this CTA issued land before its shared memory is released.
+    if (threadIdx.x == 0 && abort_flag) {
+        for (int k = 0; k < kQuantStages; ++k) {
+            const int j = it + k;  // loads issued for iterations it .. it+stages-1
+            const int blk = blockIdx.x + j * gridDim.x;
+            if (blk < total)
+                mbar_wait(smem_u32(&full[j % kQuantStages]), (j / kQuantStages) & 1, nullptr,
+                          kQuantTimeoutNs);
+        }
     }
 }
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
     const int total = p.BH * p.nblk;
-    int grid = sm_count * (2048 / kQuantThreads);
-    if (grid > total) grid = total;
-    quant_fp8_kernel<<<grid, kQuantThreads, 0, stream>>>(p);
+    cudaError_t e = cudaFuncSetAttribute(quant_fp8_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kQuantSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = total < sm_count ? total : sm_count;
+    quant_fp8_kernel<<<grid, kQuantThreads, kQuantSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

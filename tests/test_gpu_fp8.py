@@ -39,6 +39,42 @@ def test_quantizer_bit_exact_small(fa, N, d):
         np.testing.assert_array_equal(x8, r8)
 
 
+def _rounding_class_blocks():
+    """One 128 x 128 block per (amax exponent E, amax mantissa m_a): element 0 is
+    amax = (1 + m_a/128) 2^E, then +-(1 + m_x/128) 2^e for every bf16 mantissa m_x
+    and e = E-20 .. E (not above amax), the rest zero.  x / scale then runs over
+    every mantissa pair at every exponent offset, from the E4M3 subnormal range
+    (and below it) up to 448, so every rounding decision of the quotient and of
+    the E4M3 conversion is exercised."""
+    blocks = []
+    for E in (-3, 2, 9):
+        for ma in range(128):
+            amax = (1.0 + ma / 128.0) * 2.0 ** E
+            vals = [amax]
+            for e in range(E - 20, E + 1):
+                for mx in range(128):
+                    x = (1.0 + mx / 128.0) * 2.0 ** e
+                    if x <= amax:
+                        vals += [x, -x]
+            blk = np.zeros(128 * 128, dtype=np.float32)
+            blk[:len(vals)] = vals
+            blocks.append(blk.reshape(128, 128))
+    x = torch.from_numpy(np.stack(blocks))[None]          # [1, 384, 128, 128]
+    assert torch.equal(x.to(torch.bfloat16).float(), x)   # every value is a bf16
+    return x.to(torch.bfloat16)
+
+
+def test_quantizer_every_rounding_class(fa):
+    """The GPU quotient (reciprocal plus one FMA residual correction) and E4M3
+    conversion match the oracle's IEEE division bit for bit on every pair of
+    bf16 mantissas."""
+    x = _rounding_class_blocks()
+    x8, sc = _quant_gpu(fa, x)
+    r8, rsc = oracle.quantize_fp8_blockwise(x, 128)
+    np.testing.assert_array_equal(sc, rsc)
+    np.testing.assert_array_equal(x8, r8)
+
+
 def test_quantizer_zero_block(fa):
     x = torch.zeros(1, 1, 256, 128, dtype=torch.bfloat16)
     x[0, 0, 200, 5] = 3.0
