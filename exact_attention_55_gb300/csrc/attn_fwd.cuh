@@ -341,8 +341,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                         p_phase ^= 1u << i;
                         if (jj == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
                         tc_fence_after_sync();
+                        // no pv_done here: the s_full commit below also covers this PV
                         issue_pv(i, i, slot_v, jj > 1);
-                        commit(&bars->pv_done[i]);
                         if (i == 0 && !wait(&bars->kv_full[slot_k], par_k)) break;
                         issue_s(i, i, slot_k);
                         commit(&bars->s_full[i]);
@@ -540,30 +540,38 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 l += rowsum;
 
                 if (jj > 0) {
-                    // O must hold P(jj-1) V before it is rescaled, and PV(jj) must not
-                    // start before this group has seen PV(jj-1) complete.
-                    if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
-                    pv_phase ^= 1u << grp;
+                    // O must hold P(jj-1) V before it is rescaled.  With two Q tiles the
+                    // s_full commit of this step was issued after PV(jj-1) of this tile,
+                    // so its completion already implies that PV's; with one Q tile S(jj)
+                    // runs ahead of PV(jj-1) and this group waits for it explicitly.
+                    if constexpr (C::NQ == 1) {
+                        if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
+                        pv_phase ^= 1u << grp;
+                    }
                     const bool any_resc = F8 ? true : __any_sync(0xffffffffu, resc);
                     if (any_resc) {
                         tc_fence_after_sync();
                         const float f = alpha * dv_ratio;
                         const float2 f2 = make_float2(f, f);
                         const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
+                        constexpr int CH = D / 32 < 4 ? D / 32 : 4;  // chunks per batch
 #pragma unroll
-                        for (int ch = 0; ch < D / 32; ++ch) {
-                            uint32_t r[32];
-                            tmem_ld32p(o_addr + ch * 32, r);
+                        for (int c0 = 0; c0 < D / 32; c0 += CH) {
+                            uint32_t r[CH * 32];
+#pragma unroll
+                            for (int ch = 0; ch < CH; ++ch) tmem_ld32p(o_addr + (c0 + ch) * 32, r + ch * 32);
                             tmem_wait_ld_only();
-                            reg_fence32(r);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
+                            for (int ch = 0; ch < CH; ++ch) reg_fence32(r + ch * 32);
+#pragma unroll
+                            for (int e = 0; e < CH * 16; ++e) {
                                 const float2 v2 = __fmul2_rn(
                                     make_float2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), f2);
                                 r[2 * e] = __float_as_uint(v2.x);
                                 r[2 * e + 1] = __float_as_uint(v2.y);
                             }
-                            tmem_st32p(o_addr + ch * 32, r);
+#pragma unroll
+                            for (int ch = 0; ch < CH; ++ch) tmem_st32p(o_addr + (c0 + ch) * 32, r + ch * 32);
                         }
                     }
                 }

@@ -34,8 +34,12 @@ namespace gb300 {
 constexpr int kQuantThreads = 512;
 constexpr int kQuantRows = 128;
 constexpr int kQuantStages = 3;
-constexpr int kQuantStageBytes = kQuantRows * 256 * 2;  // a block of up to d = 256 bf16 columns
-constexpr int kQuantSmemBytes = 128 + kQuantStages * kQuantStageBytes + 64;
+
+// Dynamic shared memory: alignment slack, kQuantStages blocks of 128 * d bf16, barriers.
+__host__ __device__ constexpr int quant_smem_bytes(int d)
+{
+    return 128 + kQuantStages * kQuantRows * d * 2 + 64;
+}
 constexpr unsigned long long kQuantTimeoutNs = 4000000000ull;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -63,7 +67,8 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                ~uintptr_t(127));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * kQuantStageBytes);
+    const int stage_bytes = kQuantRows * p.d * 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * stage_bytes);
     __shared__ float warp_max[kQuantThreads / 32];
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -78,7 +83,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
         const uint32_t bytes = (uint32_t)block_rows(blk) * p.d * 2;
         const uint32_t bar = smem_u32(&full[stage]);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(smem_u32(smem + stage * kQuantStageBytes), x + block_base(blk), bytes, bar);
+        bulk_load(smem_u32(smem + stage * stage_bytes), x + block_base(blk), bytes, bar);
     };
 
     if (threadIdx.x == 0) {
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
             }
             break;
         }
-        const uint8_t* st = smem + stage * kQuantStageBytes;
+        const uint8_t* st = smem + stage * stage_bytes;
         const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
         float amax = 0.0f;
         for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
@@ -165,12 +170,18 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
     const int total = p.BH * p.nblk;
+    const int smem = quant_smem_bytes(p.d);
     cudaError_t e = cudaFuncSetAttribute(quant_fp8_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kQuantSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int grid = total < sm_count ? total : sm_count;
-    quant_fp8_kernel<<<grid, kQuantThreads, kQuantSmemBytes, stream>>>(p);
+    int per_sm = 1;  // CTAs that fit on one SM (two at d = 128, four at d = 64)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_fp8_kernel, kQuantThreads,
+                                                      smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long want = (long long)sm_count * per_sm;
+    const int grid = total < want ? total : (int)want;
+    quant_fp8_kernel<<<grid, kQuantThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
