@@ -444,6 +444,59 @@ def run_profile_case(args):
         sys.exit(1)
 
 
+def allowed_pairs(n, causal, window):
+    """Number of (query, key) pairs in the masks' allowed sets for one head."""
+    if window <= 0:
+        return n * (n + 1) // 2 if causal else n * n
+    w = window
+    if causal:  # sum_i (min(i, w) + 1)
+        m = min(n, w + 1)
+        return m * (m + 1) // 2 + (n - m) * (w + 1)
+    tot = 0
+    for i in range(n):
+        tot += min(n - 1, i + w) - max(0, i - w) + 1
+    return tot
+
+
+def run_sweep(args):
+    """The d x N sweep: B*N = 16384 tokens, H = 2048/d, bf16, three masks.
+    Prints one JSON line per point (TFLOP/s over allowed pairs, and the roofline bound)."""
+    import torch
+    import exact_attention_55_gb300 as fa
+    from exact_attention_55_gb300.inputs import make_qkv
+    fa.build.build()
+    fa.load_library()
+    torch.cuda.set_device(0)
+    peaks, _ = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    stream = torch.cuda.current_stream()
+    for d in (64, 128, 256):
+        for n in (512, 1024, 2048, 4096, 8192, 16384):
+            b, h = 16384 // n, 2048 // d
+            q, k, v = make_qkv(b, h, n, d, seed=7)
+            qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+            o = torch.empty_like(qd)
+            lse = torch.empty((b, h, n), dtype=torch.float32, device=qd.device)
+            for causal, window in ((False, 0), (True, 0), (True, 1024)):
+                def step():
+                    fa.attn_fwd_bf16(qd, kd, vd, scale=1.0 / math.sqrt(d), causal=causal,
+                                     window=window, o=o, lse=lse, stream=stream)
+                _, per = time_steps(step, args.steps, args.warmup, stream)
+                ms = statistics.median(per)
+                f = 4.0 * d * b * h * allowed_pairs(n, causal, window)
+                bytes_ = 8.0 * b * h * n * d + 4.0 * b * h * n
+                bound = min(peak, f / bytes_ * hbm / 1e3)  # TFLOP/s roofline at this intensity
+                t = f / (ms * 1e-3) / 1e12
+                print(json.dumps({"sweep": True, "d": d, "N": n, "B": b, "H": h,
+                                  "causal": causal, "window": window, "ms": ms,
+                                  "tflops": t, "roofline_tflops": bound,
+                                  "frac_of_roofline": t / bound}), flush=True)
+            del qd, kd, vd, o, lse
+    if fa.attn_get_device_status() != fa.ATTN_OK:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,7 +507,12 @@ def main():
     ap.add_argument("--profile", default=None,
                     choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant"],
                     help="run a small case of one kernel (for ncu) and exit")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the d x N x mask sweep (one JSON line per point) and exit")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.profile:
         run_profile_case(args)
         return

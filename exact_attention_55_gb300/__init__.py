@@ -25,7 +25,7 @@ from . import build as _build
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
     "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
-    "attn_get_device_status", "EXPORTED_SYMBOLS",
+    "attn_get_device_status", "attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK = 0
@@ -37,7 +37,7 @@ ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
     "attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
-    "attn_get_device_status",
+    "attn_get_device_status", "attn_selftest_wait_timeout",
 )
 
 _lock = threading.Lock()
@@ -76,6 +76,8 @@ def load_library(path: str | None = None):
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+        lib.attn_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -171,3 +173,9 @@ def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | Non
 def attn_get_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(load_library().attn_get_device_status(_stream_handle(stream)))
+
+
+def attn_selftest_wait_timeout(timeout_ns: int = 50_000_000, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (it records ATTN_ERR_TIMEOUT on purpose)."""
+    st = load_library().attn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream))
+    _raise_if(st, "attn_selftest_wait_timeout")

@@ -24,6 +24,18 @@ cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t st
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
 
+// A bounded wait on a barrier that no thread arrives on: exercises the timeout
+// path (give up, record the status, return) without faulting or hanging.
+__global__ void wait_timeout_kernel(int* status, unsigned long long timeout_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        if (!mbar_wait(smem_u32(&bar), 0, nullptr, timeout_ns)) atomicExch(status, kStatusTimeout);
+    }
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -235,4 +247,14 @@ extern "C" attn_status_t attn_get_device_status(void* stream)
     if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return value == 0 ? ATTN_OK : static_cast<attn_status_t>(value);
+}
+
+extern "C" attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream)
+{
+    if (timeout_ns == 0 || timeout_ns > 2000000000ull) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -109,6 +109,17 @@ const char* attn_status_string(attn_status_t status);
  */
 attn_status_t attn_get_device_status(void* stream);
 
+/*
+ * attn_selftest_wait_timeout -- diagnostic for the failure path every kernel above
+ * shares.  Launches one small kernel that waits, with the same bounded mbarrier
+ * wait the attention and quantiser kernels use, on a barrier nothing will ever
+ * arrive on.  After `timeout_ns` the wait gives up, the kernel records
+ * ATTN_ERR_TIMEOUT in the device status word and returns normally, so the
+ * context stays usable; read the word with attn_get_device_status().
+ *   timeout_ns : 1 .. 2e9 (else ATTN_ERR_INVALID_ARG)
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8",
-              "attn_status_string", "attn_get_device_status"):
+              "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout"):
         assert n in names
 
 
@@ -90,6 +90,11 @@ def test_quantizer_argument_errors(lib, args, expected):
 ])
 def test_fp8_argument_errors(lib, args, expected):
     assert lib.attn_fwd_fp8(*args, None) == expected
+
+
+def test_selftest_rejects_bad_limits_before_any_launch(lib):
+    assert lib.attn_selftest_wait_timeout(0, None) == 1
+    assert lib.attn_selftest_wait_timeout(3_000_000_000, None) == 1
 
 
 def test_binding_refuses_cpu_tensors():
