@@ -3,7 +3,8 @@
 For callers whose Q, K, V live in (pinned) host memory and who want O and LSE
 back in host memory.  The batch is cut into chunks; while the kernel runs on
 chunk c, chunk c+1 is copied to the device and chunk c-1's O and LSE are copied
-back, on three CUDA streams with two device buffers per tensor.  The arithmetic
+back, on five CUDA streams (one upload stream per input tensor, one for the
+kernel, one for the copies back) with two device buffers per tensor.  The arithmetic
 is the C-ABI call `attn_fwd_bf16` on each chunk; this module only moves memory
 and orders streams.
 """
@@ -37,7 +38,8 @@ class HostAttention:
         self.vd = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.od = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.ld = [torch.empty((self.bc, H, N), dtype=torch.float32, device=dev) for _ in range(2)]
-        self.s_in = torch.cuda.Stream(device=dev)
+        # one input stream per tensor, so the three uploads can use separate copy engines
+        self.s_ins = [torch.cuda.Stream(device=dev) for _ in range(3)]
         self.s_comp = torch.cuda.Stream(device=dev)
         self.s_out = torch.cuda.Stream(device=dev)
 
@@ -56,7 +58,8 @@ class HostAttention:
         if scale is None:
             scale = 1.0 / math.sqrt(self.d)
         caller = torch.cuda.current_stream()
-        self.s_in.wait_stream(caller)
+        for st in self.s_ins:
+            st.wait_stream(caller)
         self.s_out.wait_stream(caller)
         done_comp = [None, None]  # compute finished with buffer slot -> inputs may be overwritten
         done_out = [None, None]   # copy-back finished with buffer slot -> outputs may be overwritten
@@ -64,16 +67,18 @@ class HostAttention:
         for c in range(self.chunks):
             slot = c & 1
             b0, b1 = c * self.bc, (c + 1) * self.bc
-            with torch.cuda.stream(self.s_in):
-                if done_comp[slot] is not None:
-                    self.s_in.wait_event(done_comp[slot])
-                self.qd[slot].copy_(qh[b0:b1], non_blocking=True)
-                self.kd[slot].copy_(kh[b0:b1], non_blocking=True)
-                self.vd[slot].copy_(vh[b0:b1], non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(self.s_in)
+            evs_in = []
+            for st, dst, src in zip(self.s_ins, (self.qd, self.kd, self.vd), (qh, kh, vh)):
+                with torch.cuda.stream(st):
+                    if done_comp[slot] is not None:
+                        st.wait_event(done_comp[slot])
+                    dst[slot].copy_(src[b0:b1], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    evs_in.append(ev)
             with torch.cuda.stream(self.s_comp):
-                self.s_comp.wait_event(ev_in)
+                for ev in evs_in:
+                    self.s_comp.wait_event(ev)
                 if done_out[slot] is not None:
                     self.s_comp.wait_event(done_out[slot])
                 attn_fwd_bf16(self.qd[slot], self.kd[slot], self.vd[slot], scale=scale,
