@@ -139,6 +139,30 @@ __device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w)
 
 __device__ __forceinline__ int next_sub(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
 
+// Steps [L, R) of the unit's key-tile range that Q tile i needs: a key tile is
+// skipped for a Q tile when every (row, key) pair of it is masked (causal: all
+// keys after the tile's last row; band: all keys before its first row's window,
+// or after its last row's).  Never empty; with one Q tile the whole range.
+template <class C>
+__device__ __forceinline__ void tile_steps(const Unit& w, int i, const FwdParams& p, int& L, int& R)
+{
+    L = 0;
+    R = w.n;
+    if constexpr (C::NQ == 2) {
+        const int a = w.q0 + i * C::BM, last = a + C::BM - 1;
+        int lo_t = w.t0, hi_t = w.t0 + w.n;
+        if (p.causal) hi_t = min(hi_t, last / C::BN + 1);
+        else if (p.window > 0) hi_t = min(hi_t, (last + p.window) / C::BN + 1);
+        if (p.window > 0 && a - p.window > 0) lo_t = max(lo_t, (a - p.window) / C::BN);
+        if (lo_t >= hi_t) {
+            lo_t = w.t0 + w.n - 1;
+            hi_t = w.t0 + w.n;
+        }
+        L = lo_t - w.t0;
+        R = hi_t - w.t0;
+    }
+}
+
 __device__ __forceinline__ void raise_timeout(const FwdParams& p, FwdBars* bars)
 {
     atomicExch(p.status, kStatusTimeout);
@@ -315,15 +339,19 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
             tc_fence_after_sync();
-            // step 0: S(0) for every Q tile
+            int Lr[C::NQ], Rr[C::NQ];  // per-Q-tile step ranges
+#pragma unroll
+            for (int i = 0; i < C::NQ; ++i) tile_steps<C>(w, i, p, Lr[i], Rr[i]);
+            // step 0: S(0) for every Q tile that needs key tile 0
             {
                 const uint32_t slot = ring % C::NSLOT;
                 if (!wait(&bars->kv_full[slot], (ring / C::NSLOT) & 1)) break;
 #pragma unroll
                 for (int i = 0; i < C::NQ; ++i) {
+                    if (Lr[i] != 0) continue;
                     issue_s(i, i, slot);
                     commit(&bars->s_full[i]);
-                    if (w.n == 1) commit(&bars->q_empty[i]);
+                    if (Rr[i] == 1) commit(&bars->q_empty[i]);
                 }
                 commit(&bars->kv_empty[slot]);
                 ++ring;
@@ -335,18 +363,25 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 const uint32_t par_k = ((ring + 1) / C::NSLOT) & 1;
                 if constexpr (C::NQ == 2) {
                     if (!wait(&bars->kv_full[slot_v], par_v)) break;
+                    if (!wait(&bars->kv_full[slot_k], par_k)) break;
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
-                        if (!wait(&bars->p_full[i], (p_phase >> i) & 1)) break;
-                        p_phase ^= 1u << i;
-                        if (jj == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
-                        tc_fence_after_sync();
-                        // no pv_done here: the s_full commit below also covers this PV
-                        issue_pv(i, i, slot_v, jj > 1);
-                        if (i == 0 && !wait(&bars->kv_full[slot_k], par_k)) break;
-                        issue_s(i, i, slot_k);
-                        commit(&bars->s_full[i]);
-                        if (jj == w.n - 1) commit(&bars->q_empty[i]);
+                        const int jp = jj - 1;  // step whose P . V is due
+                        if (jp >= Lr[i] && jp < Rr[i]) {
+                            if (!wait(&bars->p_full[i], (p_phase >> i) & 1)) break;
+                            p_phase ^= 1u << i;
+                            if (jp == Lr[i] && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
+                            tc_fence_after_sync();
+                            // the s_full commit below also covers this PV; only the
+                            // tile's last PV gets its own commit (for the epilogue)
+                            issue_pv(i, i, slot_v, jp > Lr[i]);
+                            if (jp == Rr[i] - 1) commit(&bars->pv_done[i]);
+                        }
+                        if (jj >= Lr[i] && jj < Rr[i]) {
+                            issue_s(i, i, slot_k);
+                            commit(&bars->s_full[i]);
+                            if (jj == Rr[i] - 1) commit(&bars->q_empty[i]);
+                        }
                     }
                 } else {
                     const int sb = jj & 1, sp = (jj - 1) & 1;
@@ -376,11 +411,13 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < C::NQ; ++i) {
                     const int sb = (C::NQ == 2) ? i : sp;
+                    const int jp = w.n - 1;
+                    if (jp < Lr[i] || jp >= Rr[i]) continue;  // this tile finished earlier
                     if (!wait(&bars->p_full[sb], (p_phase >> sb) & 1)) break;
                     p_phase ^= 1u << sb;
-                    if (w.n == 1 && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
+                    if (jp == Lr[i] && !wait(&bars->o_empty[i], (uc & 1) ^ 1)) break;
                     tc_fence_after_sync();
-                    issue_pv(i, sb, slot_v, w.n > 1);
+                    issue_pv(i, sb, slot_v, jp > Lr[i]);
                     commit(&bars->pv_done[i]);
                 }
                 if (!ok) break;
@@ -430,8 +467,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             float dv_cur = 1.0f, q_desc = 1.0f;
             if constexpr (F8) q_desc = p.dq[(size_t)w.bh * ((p.N + 127) / 128) + a / 128];
 
+            int L, R;  // key steps this Q tile needs
+            tile_steps<C>(w, grp, p, L, R);
             float m_used = NEG_INF, l = 0.0f;
-            for (int jj = 0; jj < w.n; ++jj) {
+            for (int jj = L; jj < R; ++jj) {
                 const int t = w.t0 + jj;
                 const int c0 = t * C::BN;
                 const int sb = (C::NQ == 2) ? grp : (jj & 1);
@@ -539,7 +578,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 if constexpr (F8) rowsum *= 1.0f / float(1u << C::P8_SHIFT);
                 l += rowsum;
 
-                if (jj > 0) {
+                if (jj > L) {
                     // O must hold P(jj-1) V before it is rescaled.  With two Q tiles the
                     // s_full commit of this step was issued after PV(jj-1) of this tile,
                     // so its completion already implies that PV's; with one Q tile S(jj)
