@@ -9,10 +9,10 @@
 //   amax  = max |x|;  scale = amax / 448 (IEEE fp32 division), or 1 when amax == 0
 //   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 quotient, one rounding to E4M3)
 //
-// HBM-bound design: one persistent CTA per SM streams whole blocks (one
-// contiguous run of rows * d * 2 bytes) into a 3-stage shared-memory ring with
-// cp.async.bulk, so several blocks are in flight per SM while the threads reduce
-// and convert the current one.  Each element is read from HBM once and written
+// HBM-bound design: persistent CTAs, as many per SM as fit (two at d = 128),
+// each stream whole blocks (one contiguous run of rows * d * 2 bytes) into a
+// 3-stage shared-memory ring with cp.async.bulk, so several blocks are in flight
+// per SM while the threads reduce and convert the current one.  Each element is read from HBM once and written
 // as one byte.
 //
 // The quotient x / scale is formed from the correctly rounded reciprocal
