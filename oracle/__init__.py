@@ -22,6 +22,10 @@ Functions and the passage each follows:
   e4m3_encode / e4m3_decode  E4M3 format ([JJ] §1.5 低精度FP8)
   quantize_fp8_blockwise     per-block scaling ([WGC] §3 FP8 量化与精度保持)
   dequantize                 x ~= x8 * scale for the block, the inverse map
+  hadamard_rotate_f32        incoherent processing before quantisation ([JJ] §1
+                             item 3, 块量化和无相关处理): orthonormal Walsh-Hadamard
+                             rotation of each row, in fp32 in a fixed butterfly order
+  quantize_fp8_hadamard      the rotation followed by quantize_fp8_blockwise
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``.
 """
 from __future__ import annotations
@@ -84,6 +88,8 @@ def _load():
         lib.oracle_e4m3_encode_array.restype = None
         lib.oracle_quantize_fp8_blockwise.argtypes = [fp, u8p, fp, L, L, L, L]
         lib.oracle_quantize_fp8_blockwise.restype = None
+        lib.oracle_hadamard_rotate_f32.argtypes = [fp, fp, L, L, ctypes.c_float]
+        lib.oracle_hadamard_rotate_f32.restype = None
         _lib = lib
         return lib
 
@@ -189,6 +195,34 @@ def quantize_fp8_blockwise(x, block: int = 128):
     _load().oracle_quantize_fp8_blockwise(_ptr(x, ctypes.c_float), _ptr(x8, ctypes.c_uint8),
                                           _ptr(scales, ctypes.c_float), BH, N, d, int(block))
     return x8, scales
+
+
+def hadamard_scale(d: int) -> np.float32:
+    """c = fp32(1 / sqrt(d)): the double value rounded once to fp32."""
+    return np.float32(1.0 / np.sqrt(np.float64(d)))
+
+
+def hadamard_rotate_f32(x) -> np.ndarray:
+    """Rows of x ([..., d], bf16 or fp32 values; d a power of two) times H_d / sqrt(d),
+    computed in fp32 by the radix-2 butterfly sweep h = 1, 2, ..., d/2 and a final
+    multiply by hadamard_scale(d)."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu").to(torch.float32).numpy()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    if d < 1 or d & (d - 1):
+        raise ValueError("d must be a power of two")
+    y = np.empty_like(x)
+    _load().oracle_hadamard_rotate_f32(_ptr(x, ctypes.c_float), _ptr(y, ctypes.c_float),
+                                       x.size // d, d, hadamard_scale(d))
+    return y
+
+
+def quantize_fp8_hadamard(x, block: int = 128):
+    """Incoherent processing then per-block quantisation: quantize_fp8_blockwise of
+    hadamard_rotate_f32(x).  Dequantised values approximate x @ H_d / sqrt(d)."""
+    return quantize_fp8_blockwise(hadamard_rotate_f32(x), block)
 
 
 def dequantize(x8, scales, block: int = 128) -> np.ndarray:

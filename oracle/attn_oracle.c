@@ -303,3 +303,38 @@ void oracle_quantize_fp8_blockwise(const float* x, uint8_t* x8, float* scales, l
         scales[u] = scale;
     }
 }
+
+/*
+ * Incoherent processing before FP8 quantisation ("大模型加速-核心网络算子-Flash
+ * Attention V3", §1 item 3 and the closing summary: block quantisation together
+ * with incoherent processing, credited with a 2.6x lower FP8 error).  The pages do
+ * not spell out the transform; the reading taken here is the orthonormal
+ * Walsh-Hadamard rotation R = H_d / sqrt(d) applied to each row of Q and of K
+ * (H_d the Sylvester Hadamard matrix, entries (-1)^popcount(j & k)).  R is
+ * orthogonal, so (Q R)(K R)^T = Q K^T and the attention result is unchanged,
+ * while a large entry of a row is spread evenly over all d coordinates.
+ *
+ * The rotated values decide FP8 codes, so they are computed in fp32 in one fixed
+ * order that the GPU kernel repeats exactly: the radix-2 butterfly sweep
+ * h = 1, 2, 4, ..., d/2, each pair (i, i + h) with (i & h) == 0 becoming
+ * (a + b, a - b), then every output multiplied by c = fp32(1 / sqrt(d)).
+ * x, y: [rows, d] float32; d a power of two; y may alias x.
+ */
+void oracle_hadamard_rotate_f32(const float* x, float* y, long rows, long d, float c)
+{
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        float* v = y + r * d;
+        const float* u = x + r * d;
+        for (long j = 0; j < d; ++j) v[j] = u[j];
+        for (long h = 1; h < d; h <<= 1) {
+            for (long i = 0; i < d; ++i) {
+                if (i & h) continue;
+                const float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+        }
+        for (long j = 0; j < d; ++j) v[j] = v[j] * c;
+    }
+}
