@@ -395,6 +395,19 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     gbs = qbytes / (statistics.mean(per) * 1e-3) / 1e9
     out["quantize_fp8"] = {"GB_per_s": gbs, "ms_3_tensors": statistics.mean(per),
                            "frac_of_hbm": gbs / hbm, "bytes": qbytes}
+    # incoherent processing: Q and K rotated (Walsh-Hadamard) before quantisation, V plain
+    hbufs = [(torch.empty(q2d.shape, dtype=torch.uint8, device=dev),
+              torch.empty((B, H, nb), dtype=torch.float32, device=dev)) for _ in range(2)]
+
+    def quant_hadamard_step():
+        for x, (x8, sc) in zip((q2d, k2d), hbufs):
+            fa.attn_quantize_fp8_hadamard(x, x8=x8, scales=sc, stream=stream)
+        fa.attn_quantize_fp8_blockwise(v2d, x8=bufs[2][0], scales=bufs[2][1], stream=stream)
+
+    ms, per = time_steps(quant_hadamard_step, reps, 3, stream)
+    gbs = qbytes / (statistics.mean(per) * 1e-3) / 1e9
+    out["quantize_fp8_hadamard_qk"] = {"GB_per_s": gbs, "ms_3_tensors": statistics.mean(per),
+                                       "frac_of_hbm": gbs / hbm, "bytes": qbytes}
     (q8, sq), (k8, sk), (v8, sv) = bufs
     peak8 = float(peaks.get("fp8_tflops",
                             FP8_NOMINAL_RATIO * float(peaks.get("bf16_tflops", 1900.0))))
@@ -422,10 +435,10 @@ def run_profile_case(args):
     fa.load_library()
     torch.cuda.set_device(0)
     b, h, n, d = 2, 16, 8192, 128       # 3 x 67 MB of Q/K/V: above L2 together
-    if args.profile == "quant":
+    if args.profile.startswith("quant"):
         b = 8                           # one 537 MB tensor: above L2 on its own
     q, k, v = make_qkv(b, h, n, d, seed=0, outliers=args.profile.startswith("fp8") or
-                       args.profile == "quant")
+                       args.profile.startswith("quant"))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     scale = 1.0 / math.sqrt(d)
     if args.profile in ("bf16", "bf16_causal"):
@@ -434,6 +447,9 @@ def run_profile_case(args):
     elif args.profile == "quant":
         def run():
             fa.attn_quantize_fp8_blockwise(qd)
+    elif args.profile == "quant_hadamard":
+        def run():
+            fa.attn_quantize_fp8_hadamard(qd)
     else:
         qs = [fa.attn_quantize_fp8_blockwise(t) for t in (qd, kd, vd)]
 
@@ -510,7 +526,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
     ap.add_argument("--profile", default=None,
-                    choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant"],
+                    choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant",
+                             "quant_hadamard"],
                     help="run a small case of one kernel (for ncu) and exit")
     ap.add_argument("--sweep", action="store_true",
                     help="time the d x N x mask sweep (one JSON line per point) and exit")

@@ -10,6 +10,7 @@ raises.
     o, lse = fa.attn_fwd_bf16(q, k, v, causal=True)          # q, k, v: cuda bf16 [B,H,N,d]
     q8, sq = fa.attn_quantize_fp8_blockwise(q)               # E4M3 codes + per-block scales
     o8, lse8 = fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv)
+    q8h, sqh = fa.attn_quantize_fp8_hadamard(q)              # rotate rows, then quantise (Q, K)
 """
 from __future__ import annotations
 
@@ -24,8 +25,9 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
-    "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
-    "attn_get_device_status", "attn_selftest_wait_timeout", "EXPORTED_SYMBOLS",
+    "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
+    "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
+    "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK = 0
@@ -36,8 +38,9 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8", "attn_status_string",
-    "attn_get_device_status", "attn_selftest_wait_timeout",
+    "attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard",
+    "attn_fwd_fp8", "attn_status_string", "attn_get_device_status",
+    "attn_selftest_wait_timeout",
 )
 
 _lock = threading.Lock()
@@ -70,6 +73,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_bf16.restype = i
         lib.attn_quantize_fp8_blockwise.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.attn_quantize_fp8_blockwise.restype = i
+        lib.attn_quantize_fp8_hadamard.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+        lib.attn_quantize_fp8_hadamard.restype = i
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_fp8.restype = i
         lib.attn_status_string.argtypes = [i]
@@ -128,19 +133,44 @@ def attn_fwd_bf16(q, k, v, scale: float | None = None, causal: bool = False, win
     return o, lse
 
 
+def _quant_outputs(x, block, x8, scales):
+    B, H, N, d = x.shape
+    nblk = (N + block - 1) // block
+    if x8 is None:
+        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+    elif (x8.dtype != torch.uint8 or tuple(x8.shape) != (B, H, N, d) or x8.device != x.device
+          or not x8.is_contiguous()):
+        raise TypeError(f"x8 must be a contiguous uint8 tensor of shape {(B, H, N, d)} on {x.device}")
+    if scales is None:
+        scales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    elif (scales.dtype != torch.float32 or tuple(scales.shape) != (B, H, nblk)
+          or scales.device != x.device or not scales.is_contiguous()):
+        raise TypeError(f"scales must be a contiguous float32 tensor of shape {(B, H, nblk)} on {x.device}")
+    return x8, scales
+
+
 def attn_quantize_fp8_blockwise(x, block: int = 128, x8=None, scales=None, stream=None):
     """Per-(head, 128-row block) E4M3 quantisation; returns (x8 uint8 codes, fp32 scales)."""
     _check_bhnd("x", x, torch.bfloat16)
     B, H, N, d = x.shape
-    if x8 is None:
-        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
-    if scales is None:
-        scales = torch.empty((B, H, (N + block - 1) // block), dtype=torch.float32,
-                             device=x.device)
+    x8, scales = _quant_outputs(x, block, x8, scales)
     st = load_library().attn_quantize_fp8_blockwise(x.data_ptr(), x8.data_ptr(),
                                                     scales.data_ptr(), B, H, N, d, int(block),
                                                     _stream_handle(stream))
     _raise_if(st, "attn_quantize_fp8_blockwise")
+    return x8, scales
+
+
+def attn_quantize_fp8_hadamard(x, block: int = 128, x8=None, scales=None, stream=None):
+    """Rows of x times the orthonormal Walsh-Hadamard matrix, then per-block E4M3
+    quantisation (for Q and K); returns (x8 uint8 codes, fp32 scales)."""
+    _check_bhnd("x", x, torch.bfloat16)
+    B, H, N, d = x.shape
+    x8, scales = _quant_outputs(x, block, x8, scales)
+    st = load_library().attn_quantize_fp8_hadamard(x.data_ptr(), x8.data_ptr(),
+                                                   scales.data_ptr(), B, H, N, d, int(block),
+                                                   _stream_handle(stream))
+    _raise_if(st, "attn_quantize_fp8_hadamard")
     return x8, scales
 
 

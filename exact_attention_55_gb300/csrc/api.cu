@@ -193,12 +193,13 @@ extern "C" attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void
     return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s);
 }
 
-extern "C" attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales, int B,
-                                                     int H, int N, int d, int block, void* stream)
+static attn_status_t quantize(const void* x, void* x8, float* scales, int B, int H, int N, int d,
+                              int block, bool rotate, void* stream)
 {
     if (!x || !x8 || !scales) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
     if (block != 128 || d % 16 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
+    if (rotate && d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
     if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scales, 4)) return ATTN_ERR_MISALIGNED;
     const long long BH = (long long)B * H;
     const long long nblk = (N + 127) / 128;
@@ -215,9 +216,23 @@ extern "C" attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, fl
     p.N = N;
     p.d = d;
     p.nblk = (int)nblk;
+    p.rotate = rotate ? 1 : 0;
+    p.rot_c = (float)(1.0 / sqrt((double)d));
     if (launch_quant_fp8(p, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales, int B,
+                                                     int H, int N, int d, int block, void* stream)
+{
+    return quantize(x, x8, scales, B, H, N, d, block, false, stream);
+}
+
+extern "C" attn_status_t attn_quantize_fp8_hadamard(const void* x, void* x8, float* scales, int B,
+                                                    int H, int N, int d, int block, void* stream)
+{
+    return quantize(x, x8, scales, B, H, N, d, block, true, stream);
 }
 
 extern "C" const char* attn_status_string(attn_status_t status)

@@ -35,6 +35,8 @@ struct QuantParams {
     int* status;          // device status word (timeouts)
     int BH, N, d;
     int nblk;             // ceil(N / 128)
+    int rotate;           // 1: Walsh-Hadamard rotation of each row before quantising
+    float rot_c;          // rotation normalisation fp32(1 / sqrt(d))
 };
 
 }  // namespace gb300

@@ -15,6 +15,17 @@
 // per SM while the threads reduce and convert the current one.  Each element is read from HBM once and written
 // as one byte.
 //
+// With rotation (incoherent processing, "大模型加速-核心网络算子-Flash Attention
+// V3" §1 item 3: 块量化和无相关处理), each row is first multiplied by the
+// orthonormal Walsh-Hadamard matrix H_d / sqrt(d), computed in fp32 as the
+// radix-2 butterfly sweep h = 1, 2, ..., d/2 -- each pair (i, i + h), (i & h) == 0,
+// becomes (a + b, a - b) -- followed by one multiply by c = fp32(1 / sqrt(d)); the
+// block's amax and codes are then taken over the rotated values.  Four threads
+// share a row: thread q holds the 16-byte chunks q, q + 4, q + 8, ... of it, so
+// element index bits 0-2 and 5+ are inside a thread and bits 3-4 are the lane's
+// quarter (stages h = 8, 16 exchange with lanes q ^ 1, q ^ 2).  Every butterfly
+// rounds exactly as in that sweep, so the codes do not depend on the split.
+//
 // The quotient x / scale is formed from the correctly rounded reciprocal
 // y = RN(1/scale) with one residual correction, q = RN(x*y), r = x - scale*q
 // (exact with an FMA), q' = RN(q + r*y) -- Markstein's final division step
@@ -62,6 +73,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// DR = 0: plain per-block quantisation (any d); DR = d in {64, 128, 256}: rotate first.
+template <int DR>
 __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const QuantParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -110,39 +123,125 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
             break;
         }
         const uint8_t* st = smem + stage * stage_bytes;
-        const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
-        float amax = 0.0f;
-        for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
-            const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        // block amax over all threads (every thread passes its own partial)
+        auto block_amax = [&](float amax) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
-        }
+            for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+            if (lane == 0) warp_max[warp] = amax;
+            __syncthreads();
+            amax = warp_max[0];
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
-        if (lane == 0) warp_max[warp] = amax;
-        __syncthreads();
-        amax = warp_max[0];
+            for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+            return amax;
+        };
+        float scale;
+        if constexpr (DR == 0) {
+            const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
+            float amax = 0.0f;
+            for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+                const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-        const float scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        const float y = __frcp_rn(scale);
-
-        uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
-        for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
-            const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t out[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const uint32_t lo = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
-                                                div_by_scale(bf16_hi(w[2 * e]), scale, y));
-                const uint32_t hi = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
-                                                div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
-                out[e] = lo | (hi << 16);
+                for (int e = 0; e < 4; ++e)
+                    amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
             }
-            __stcs(dst + g, make_uint2(out[0], out[1]));
+            amax = block_amax(amax);
+            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            const float y = __frcp_rn(scale);
+
+            uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
+            for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+                const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t out[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t lo = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
+                                                    div_by_scale(bf16_hi(w[2 * e]), scale, y));
+                    const uint32_t hi = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
+                                                    div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
+                    out[e] = lo | (hi << 16);
+                }
+                __stcs(dst + g, make_uint2(out[0], out[1]));
+            }
+        } else {
+            static_assert(DR == 64 || DR == 128 || DR == 256, "rotated head dim");
+            static_assert(kQuantThreads == 4 * kQuantRows, "four threads per row");
+            constexpr int E = DR / 4;    // elements per thread
+            constexpr int NCH = E / 8;   // 16-byte chunks per thread
+            const int r = threadIdx.x >> 2, q = threadIdx.x & 3;
+            const bool live = r < block_rows(blk);
+            // v[8 m + j] holds element 32 m + 8 q + j of row r
+            float v[E];
+#pragma unroll
+            for (int m = 0; m < NCH; ++m) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 32 * m + 8 * q) * 2);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * m + 2 * e] = bf16_lo(ww[e]);
+                    v[8 * m + 2 * e + 1] = bf16_hi(ww[e]);
+                }
+            }
+            // h = 1, 2, 4: inside each chunk
+#pragma unroll
+            for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+                for (int m = 0; m < NCH; ++m)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (!(j & h)) {
+                            const float a = v[8 * m + j], b = v[8 * m + j + h];
+                            v[8 * m + j] = __fadd_rn(a, b);
+                            v[8 * m + j + h] = __fsub_rn(a, b);
+                        }
+            // h = 8, 16: across the row's four lanes
+#pragma unroll
+            for (int lb = 0; lb < 2; ++lb) {
+                const bool upper = (q >> lb) & 1;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float o = __shfl_xor_sync(0xffffffffu, v[e], 1 << lb);
+                    v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+                }
+            }
+            // h = 32, 64, ...: across chunks of a thread
+#pragma unroll
+            for (int hm = 1; hm < NCH; hm <<= 1)
+#pragma unroll
+                for (int m = 0; m < NCH; ++m)
+                    if (!(m & hm))
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float a = v[8 * m + j], b = v[8 * (m + hm) + j];
+                            v[8 * m + j] = __fadd_rn(a, b);
+                            v[8 * (m + hm) + j] = __fsub_rn(a, b);
+                        }
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                v[e] = __fmul_rn(v[e], p.rot_c);
+                amax = fmaxf(amax, fabsf(v[e]));
+            }
+            amax = block_amax(amax);
+            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            const float y = __frcp_rn(scale);
+            if (live) {
+                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;
+#pragma unroll
+                for (int m = 0; m < NCH; ++m) {
+                    uint32_t out[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float* u = v + 8 * m + 4 * e;
+                        const uint32_t lo = pack_e4m3x2(div_by_scale(u[0], scale, y), div_by_scale(u[1], scale, y));
+                        const uint32_t hi = pack_e4m3x2(div_by_scale(u[2], scale, y), div_by_scale(u[3], scale, y));
+                        out[e] = lo | (hi << 16);
+                    }
+                    __stcs(reinterpret_cast<uint2*>(row8 + 32 * m), make_uint2(out[0], out[1]));
+                }
+            }
         }
         if (threadIdx.x == 0) p.scales[blk] = scale;
         // every thread is done with this stage (and with warp_max) before it is refilled
@@ -167,22 +266,33 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
     }
 }
 
-cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
+template <int DR>
+static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
     const int total = p.BH * p.nblk;
     const int smem = quant_smem_bytes(p.d);
-    cudaError_t e = cudaFuncSetAttribute(quant_fp8_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kernel = quant_fp8_kernel<DR>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 1;  // CTAs that fit on one SM (two at d = 128, four at d = 64)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_fp8_kernel, kQuantThreads,
-                                                      smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQuantThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long want = (long long)sm_count * per_sm;
     const int grid = total < want ? total : (int)want;
-    quant_fp8_kernel<<<grid, kQuantThreads, smem, stream>>>(p);
+    kernel<<<grid, kQuantThreads, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
+{
+    if (!p.rotate) return launch_quant<0>(p, sm_count, stream);
+    switch (p.d) {
+    case 64: return launch_quant<64>(p, sm_count, stream);
+    case 128: return launch_quant<128>(p, sm_count, stream);
+    case 256: return launch_quant<256>(p, sm_count, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace gb300

@@ -81,6 +81,29 @@ attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales
                                           int N, int d, int block, void* stream);
 
 /*
+ * attn_quantize_fp8_hadamard -- incoherent processing, then per-block FP8-E4M3
+ * quantisation.
+ *
+ * [JJ] §1 item 3 and its summary (块量化和无相关处理: block quantisation together
+ * with incoherent processing, credited with a 2.6x lower FP8 error).  The pages do
+ * not spell out the transform; here each row of x is multiplied by the
+ * orthonormal Walsh-Hadamard matrix H_d / sqrt(d) (H_d[j][k] = (-1)^popcount(j & k))
+ * and the result is quantised exactly as attn_quantize_fp8_blockwise does.  Apply
+ * it to Q and K, not V: the rotation is orthogonal, so scores computed from the
+ * rotated Q and K equal Q K^T, while an outlier in a row is spread over all d
+ * coordinates and the block scale no longer has to cover it alone.
+ * The rotated values are computed in fp32: the butterfly sweep h = 1, 2, ..., d/2
+ * (each pair i, i + h with (i & h) == 0 becomes a + b, a - b, in that order of
+ * stages), then a multiply by fp32(1 / sqrt(d)) (the double 1/sqrt(d) rounded
+ * once).  Codes and scales are therefore a pure function of x.
+ *   x, x8, scales, block : as attn_quantize_fp8_blockwise
+ *   d in {64, 128, 256} (else ATTN_ERR_UNSUPPORTED)
+ * The outputs feed attn_fwd_fp8 unchanged (descale_q / descale_k = these scales).
+ */
+attn_status_t attn_quantize_fp8_hadamard(const void* x, void* x8, float* scales, int B, int H,
+                                         int N, int d, int block, void* stream);
+
+/*
  * attn_fwd_fp8 -- the forward pass with both matmuls on FP8-E4M3 operands.
  *
  * [WGC] §3 FP8 量化与精度保持 (FP8 inputs, FP32 accumulation, 16-bit output) and
@@ -90,8 +113,10 @@ attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales
  *                   (x ~= x8 * descale for the 128-row block of the row)
  *   o, lse, scale, causal, window : as attn_fwd_bf16
  *   d in {128, 256}; N % 128 == 0 (else ATTN_ERR_UNSUPPORTED)
- * Scores are descaled per (query block, key block) inside the softmax; P is
- * rounded to E4M3 after a per-key-block factor that carries the V descale.
+ * Scores are descaled per (query block, key block) inside the softmax.  P is
+ * rounded to E4M3 as p * 2^8 (p <= 1 against the exact running maximum); the V
+ * descale of each key block is applied to the fp32 O accumulator, which is
+ * rescaled by alpha * dv(t-1) / dv(t) before P(t) V8(t) is added.
  */
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                            const float* descale_q, const float* descale_k,
