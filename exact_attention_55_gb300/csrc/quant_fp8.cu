@@ -12,19 +12,20 @@
 // HBM-bound design: persistent CTAs, as many per SM as fit (two at d = 128),
 // each stream whole blocks (one contiguous run of rows * d * 2 bytes) into a
 // 3-stage shared-memory ring with cp.async.bulk, so several blocks are in flight
-// per SM while the threads reduce and convert the current one.  Each element is read from HBM once and written
-// as one byte.
+// per SM while the threads reduce and convert the current one.  Each element is
+// read from HBM once and written as one byte.
 //
 // With rotation (incoherent processing, "大模型加速-核心网络算子-Flash Attention
 // V3" §1 item 3: 块量化和无相关处理), each row is first multiplied by the
 // orthonormal Walsh-Hadamard matrix H_d / sqrt(d), computed in fp32 as the
 // radix-2 butterfly sweep h = 1, 2, ..., d/2 -- each pair (i, i + h), (i & h) == 0,
 // becomes (a + b, a - b) -- followed by one multiply by c = fp32(1 / sqrt(d)); the
-// block's amax and codes are then taken over the rotated values.  Four threads
-// share a row: thread q holds the 16-byte chunks q, q + 4, q + 8, ... of it, so
-// element index bits 0-2 and 5+ are inside a thread and bits 3-4 are the lane's
-// quarter (stages h = 8, 16 exchange with lanes q ^ 1, q ^ 2).  Every butterfly
-// rounds exactly as in that sweep, so the codes do not depend on the split.
+// block's amax and codes are then taken over the rotated values.  TPR threads
+// share a row (TPR = 4): thread q holds the 16-byte
+// chunks q, q + TPR, q + 2 TPR, ... of it, so element index bits 0-2 and the bits
+// above the chunk-lane bits are inside a thread, while the stages h = 8 .. 4 TPR
+// exchange with lanes q ^ 1 and q ^ 2 by shuffles.  Every butterfly rounds
+// exactly as in the sweep, so the codes do not depend on the split.
 //
 // The quotient x / scale is formed from the correctly rounded reciprocal
 // y = RN(1/scale) with one residual correction, q = RN(x*y), r = x - scale*q
@@ -42,7 +43,6 @@
 
 namespace gb300 {
 
-constexpr int kQuantThreads = 512;
 constexpr int kQuantRows = 128;
 constexpr int kQuantStages = 3;
 
@@ -73,16 +73,48 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// RN(x / s) for two values at once (the same three roundings as div_by_scale).
+__device__ __forceinline__ float2 div2_by_scale(float2 x, float2 s_neg, float2 y)
+{
+    const float2 q = __fmul2_rn(x, y);
+    const float2 r = __ffma2_rn(q, s_neg, x);  // x - q s, exact
+    const float2 c = __ffma2_rn(r, y, q);
+    // c equals q when r == 0, except that q = -0 (x = -0) would come back as +0;
+    // the quotient's sign is x's in every case
+    return make_float2(copysignf(c.x, x.x), copysignf(c.y, x.y));
+}
+
+// a + b and a - b of two pairs, each rounded once (a - b as fma(b, -1, a)).
+__device__ __forceinline__ void butterfly2(float& a0, float& a1, float& b0, float& b1)
+{
+    const float2 a = make_float2(a0, a1), b = make_float2(b0, b1);
+    const float2 sum = __fadd2_rn(a, b);
+    const float2 dif = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+    a0 = sum.x; a1 = sum.y;
+    b0 = dif.x; b1 = dif.y;
+}
+
+// Launch shape per variant: 512 threads (four per row of a 128-row block); for the
+// rotated d <= 128 variants the registers are capped so two CTAs share an SM.
+// (Two threads per row -- one shuffle stage fewer, half the warps -- measured slower.)
+template <int DR> struct QuantShape {
+    static constexpr int TPR = 4;
+    static constexpr int kThreads = (DR == 0) ? 512 : kQuantRows * TPR;
+    static constexpr int kMinBlocks = (DR > 0 && DR <= 128) ? 2 : 1;
+};
+
 // DR = 0: plain per-block quantisation (any d); DR = d in {64, 128, 256}: rotate first.
 template <int DR>
-__global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const QuantParams p)
+__global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMinBlocks)
+    quant_fp8_kernel(const QuantParams p)
 {
+    constexpr int kThreads = QuantShape<DR>::kThreads;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                ~uintptr_t(127));
     const int stage_bytes = kQuantRows * p.d * 2;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * stage_bytes);
-    __shared__ float warp_max[kQuantThreads / 32];
+    __shared__ float warp_max[kThreads / 32];
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = p.BH * p.nblk;
@@ -131,14 +163,14 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
             __syncthreads();
             amax = warp_max[0];
 #pragma unroll
-            for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+            for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
             return amax;
         };
         float scale;
         if constexpr (DR == 0) {
             const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
             float amax = 0.0f;
-            for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+            for (int g = threadIdx.x; g < nchunk; g += kThreads) {
                 const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -150,7 +182,7 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
             const float y = __frcp_rn(scale);
 
             uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
-            for (int g = threadIdx.x; g < nchunk; g += kQuantThreads) {
+            for (int g = threadIdx.x; g < nchunk; g += kThreads) {
                 const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 uint32_t out[2];
@@ -166,17 +198,18 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
             }
         } else {
             static_assert(DR == 64 || DR == 128 || DR == 256, "rotated head dim");
-            static_assert(kQuantThreads == 4 * kQuantRows, "four threads per row");
-            constexpr int E = DR / 4;    // elements per thread
-            constexpr int NCH = E / 8;   // 16-byte chunks per thread
-            const int r = threadIdx.x >> 2, q = threadIdx.x & 3;
+            constexpr int TPR = QuantShape<DR>::TPR;  // threads per row
+            constexpr int E = DR / TPR;               // elements per thread
+            constexpr int NCH = E / 8;                // 16-byte chunks per thread
+            const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
             const bool live = r < block_rows(blk);
-            // v[8 m + j] holds element 32 m + 8 q + j of row r
+            // v[8 m + j] holds element 8 (TPR m + q) + j of row r
             float v[E];
 #pragma unroll
             for (int m = 0; m < NCH; ++m) {
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 32 * m + 8 * q) * 2);
+                if (live)
+                    w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * m + q)) * 2);
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -184,62 +217,71 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quant_fp8_kernel(const Quant
                     v[8 * m + 2 * e + 1] = bf16_hi(ww[e]);
                 }
             }
-            // h = 1, 2, 4: inside each chunk
+            // h = 1: neighbours inside a pair of registers
 #pragma unroll
-            for (int h = 1; h < 8; h <<= 1)
+            for (int e = 0; e < E; e += 2) {
+                const float a = v[e], b = v[e + 1];
+                v[e] = __fadd_rn(a, b);
+                v[e + 1] = __fsub_rn(a, b);
+            }
+            // h = 2, 4: inside each chunk, two butterflies per packed instruction
+#pragma unroll
+            for (int h = 2; h < 8; h <<= 1)
 #pragma unroll
                 for (int m = 0; m < NCH; ++m)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (!(j & h)) {
-                            const float a = v[8 * m + j], b = v[8 * m + j + h];
-                            v[8 * m + j] = __fadd_rn(a, b);
-                            v[8 * m + j + h] = __fsub_rn(a, b);
-                        }
-            // h = 8, 16: across the row's four lanes
+                    for (int j = 0; j < 8; j += 2)
+                        if (!(j & h)) butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * m + j + h], v[8 * m + j + h + 1]);
+            // h = 8, 16, ..., 4 TPR: across the row's lanes; the lower lane keeps v + o
+            // and the upper one o - v, both as fma(v, +-1, o)
 #pragma unroll
-            for (int lb = 0; lb < 2; ++lb) {
-                const bool upper = (q >> lb) & 1;
+            for (int lb = 0; (1 << lb) < TPR; ++lb) {
+                const float sg = ((q >> lb) & 1) ? -1.0f : 1.0f;
+                const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float o = __shfl_xor_sync(0xffffffffu, v[e], 1 << lb);
-                    v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
+                for (int e = 0; e < E; e += 2) {
+                    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], 1 << lb),
+                                                 __shfl_xor_sync(0xffffffffu, v[e + 1], 1 << lb));
+                    const float2 t = __ffma2_rn(make_float2(v[e], v[e + 1]), sg2, o);
+                    v[e] = t.x;
+                    v[e + 1] = t.y;
                 }
             }
-            // h = 32, 64, ...: across chunks of a thread
+            // h = 8 TPR, 16 TPR, ...: across chunks of a thread
 #pragma unroll
             for (int hm = 1; hm < NCH; hm <<= 1)
 #pragma unroll
                 for (int m = 0; m < NCH; ++m)
                     if (!(m & hm))
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float a = v[8 * m + j], b = v[8 * (m + hm) + j];
-                            v[8 * m + j] = __fadd_rn(a, b);
-                            v[8 * (m + hm) + j] = __fsub_rn(a, b);
-                        }
+                        for (int j = 0; j < 8; j += 2)
+                            butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
             float amax = 0.0f;
+            const float2 c2 = make_float2(p.rot_c, p.rot_c);
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                v[e] = __fmul_rn(v[e], p.rot_c);
-                amax = fmaxf(amax, fabsf(v[e]));
+            for (int e = 0; e < E; e += 2) {
+                const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
+                v[e] = t.x;
+                v[e + 1] = t.y;
+                amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
             }
             amax = block_amax(amax);
             scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
             const float y = __frcp_rn(scale);
+            const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
             if (live) {
-                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;
+                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;  // chunk TPR m + q
 #pragma unroll
                 for (int m = 0; m < NCH; ++m) {
                     uint32_t out[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const float* u = v + 8 * m + 4 * e;
-                        const uint32_t lo = pack_e4m3x2(div_by_scale(u[0], scale, y), div_by_scale(u[1], scale, y));
-                        const uint32_t hi = pack_e4m3x2(div_by_scale(u[2], scale, y), div_by_scale(u[3], scale, y));
-                        out[e] = lo | (hi << 16);
+                        const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
+                        const float2 b = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
+                        out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(b.x, b.y) << 16);
                     }
-                    __stcs(reinterpret_cast<uint2*>(row8 + 32 * m), make_uint2(out[0], out[1]));
+                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * TPR * m), make_uint2(out[0], out[1]));
                 }
             }
         }
@@ -275,12 +317,13 @@ static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 1;  // CTAs that fit on one SM (two at d = 128, four at d = 64)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQuantThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, QuantShape<DR>::kThreads,
+                                                      smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long want = (long long)sm_count * per_sm;
     const int grid = total < want ? total : (int)want;
-    kernel<<<grid, kQuantThreads, smem, stream>>>(p);
+    kernel<<<grid, QuantShape<DR>::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
