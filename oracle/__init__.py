@@ -26,6 +26,9 @@ Functions and the passage each follows:
                              item 3, 块量化和无相关处理): orthonormal Walsh-Hadamard
                              rotation of each row, in fp32 in a fixed butterfly order
   quantize_fp8_hadamard      the rotation followed by quantize_fp8_blockwise
+  attn_varlen_f64            variable-length sequences packed without padding ([YT]
+                             §1.1 可变序列长度): each sequence attends only within
+                             itself, masks relative to its own first token
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``.
 """
 from __future__ import annotations
@@ -147,6 +150,29 @@ def attn_rows_f64(q, k, v, rows, scale: float, causal: bool = False, window: int
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(nthreads))
     if return_threads:
         return o, lse, nt
+    return o, lse
+
+
+def attn_varlen_f64(q, k, v, cu_seqlens, scale: float, causal: bool = False, window: int = 0):
+    """Packed variable-length sequences.  q, k, v: [T, H, d] (bf16 or float values),
+    cu_seqlens: S + 1 non-decreasing token offsets with cu[0] = 0 and cu[S] = T;
+    sequence s is tokens [cu[s], cu[s+1]).  Returns (O [T, H, d], LSE [H, T]) float64:
+    attn_f64 of each sequence on its own (its rows, its keys, its mask)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T, H, d = q.shape
+    if cu[0] != 0 or cu[-1] != T or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise from 0 to T")
+    o = np.zeros((T, H, d))
+    lse = np.zeros((H, T))
+    for a, b in zip(cu, cu[1:]):
+        if b == a:
+            continue
+        # [n, H, d] -> [H, n, d] for the per-head definition
+        oh, lh = attn_f64(q[a:b].transpose(1, 0, 2), k[a:b].transpose(1, 0, 2),
+                          v[a:b].transpose(1, 0, 2), scale, causal=causal, window=window)
+        o[a:b] = oh.transpose(1, 0, 2)
+        lse[:, a:b] = lh
     return o, lse
 
 
