@@ -11,6 +11,7 @@ raises.
     q8, sq = fa.attn_quantize_fp8_blockwise(q)               # E4M3 codes + per-block scales
     o8, lse8 = fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv)
     q8h, sqh = fa.attn_quantize_fp8_hadamard(q)              # rotate rows, then quantise (Q, K)
+    o, lse = fa.attn_fwd_bf16_varlen(qp, kp, vp, cu, max_len) # packed [T, H, d], int32 offsets
 """
 from __future__ import annotations
 
@@ -25,6 +26,7 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
+    "attn_fwd_bf16_varlen",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
@@ -38,7 +40,8 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard",
+    "attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_quantize_fp8_blockwise",
+    "attn_quantize_fp8_hadamard",
     "attn_fwd_fp8", "attn_status_string", "attn_get_device_status",
     "attn_selftest_wait_timeout",
 )
@@ -71,6 +74,8 @@ def load_library(path: str | None = None):
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_bf16.restype = i
+        lib.attn_fwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        lib.attn_fwd_bf16_varlen.restype = i
         lib.attn_quantize_fp8_blockwise.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.attn_quantize_fp8_blockwise.restype = i
         lib.attn_quantize_fp8_hadamard.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -106,6 +111,12 @@ def _check_bhnd(name, t, dtype):
         raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
 
 
+def _check_out(t, shape, dtype, device, name):
+    if (not isinstance(t, torch.Tensor) or t.dtype != dtype or tuple(t.shape) != tuple(shape)
+            or t.device != device or not t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+
+
 def _raise_if(status: int, where: str):
     if status != ATTN_OK:
         raise AttnError(status, where)
@@ -126,10 +137,46 @@ def attn_fwd_bf16(q, k, v, scale: float | None = None, causal: bool = False, win
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_bhnd("o", o, torch.bfloat16)
+    _check_out(o, q.shape, torch.bfloat16, q.device, "o")
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
     st = load_library().attn_fwd_bf16(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                       lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
                                       int(window), _stream_handle(stream))
     _raise_if(st, "attn_fwd_bf16")
+    return o, lse
+
+
+def attn_fwd_bf16_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
+                         causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
+    """Packed variable-length sequences: q, k, v bf16 [T, H, d]; cu_seqlens int32 [S + 1]
+    on the same device (sequence s = tokens cu[s] .. cu[s+1]-1); max_seqlen >= every
+    length.  Returns O [T, H, d] and the natural-log LSE [H, T]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{n} must be a CUDA bf16 tensor")
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous [T, H, d] tensor")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if (not isinstance(cu_seqlens, torch.Tensor) or cu_seqlens.dtype != torch.int32
+            or cu_seqlens.device != q.device or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2
+            or not cu_seqlens.is_contiguous()):
+        raise TypeError("cu_seqlens must be a contiguous int32 [S + 1] tensor on q's device")
+    T, H, d = q.shape
+    S = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    _check_out(o, (T, H, d), torch.bfloat16, q.device, "o")
+    _check_out(lse, (H, T), torch.float32, q.device, "lse")
+    st = load_library().attn_fwd_bf16_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                             lse.data_ptr(), cu_seqlens.data_ptr(), S,
+                                             int(max_seqlen), T, H, d, float(scale),
+                                             int(bool(causal)), int(window), _stream_handle(stream))
+    _raise_if(st, "attn_fwd_bf16_varlen")
     return o, lse
 
 
@@ -181,6 +228,8 @@ def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | Non
         if t.dtype == torch.float8_e4m3fn:
             t = t.view(torch.uint8)
         _check_bhnd(n, t, torch.uint8)
+    if k8.shape != q8.shape or v8.shape != q8.shape:
+        raise ValueError("q8, k8, v8 must have the same shape")
     B, H, N, d = q8.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -188,9 +237,10 @@ def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | Non
         o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _check_out(o, (B, H, N, d), torch.bfloat16, q8.device, "o")
+    _check_out(lse, (B, H, N), torch.float32, q8.device, "lse")
     for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
-        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-            raise TypeError(f"{n} must be a contiguous cuda float32 tensor")
+        _check_out(t, (B, H, (N + 127) // 128), torch.float32, q8.device, n)
     st = load_library().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(),
                                      descale_q.data_ptr(), descale_k.data_ptr(),
                                      descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,

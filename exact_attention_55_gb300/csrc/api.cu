@@ -98,6 +98,61 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a packed [T, H, d] tensor: dims (d, H, T) innermost first (strides
+// grow outward), boxes of (128 bytes of d) x 1 head x box_rows tokens -- the same
+// shared-memory layout as the batched map's boxes.  Tokens past T read as zero.
+bool encode_3d_packed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                      int d, int H, int T, int box_rows)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)H * d * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), 1, (cuuint32_t)box_rows};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const int* cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
+                             float scale, int causal, int window, cudaStream_t stream)
+{
+    using C = FwdCfg<D, false>;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    alignas(64) CUtensorMap mq, mk, mv;
+    if (!encode_3d_packed(&mq, q, dt, C::EB, D, H, T, C::BM) ||
+        !encode_3d_packed(&mk, k, dt, C::EB, D, H, T, C::BN) ||
+        !encode_3d_packed(&mv, v, dt, C::EB, D, H, T, C::BN))
+        return ATTN_ERR_CUDA;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.o = o;
+    p.lse = lse;
+    p.status = dev->status;
+    p.BH = num_seqs * H;
+    p.N = max_seqlen;
+    p.num_qblk = (max_seqlen + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+    const long long units = (long long)num_seqs * H * ((p.num_qblk + 1) / 2);
+    if (2 * units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    p.num_units = (int)units;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    p.timeout_ns = kWaitTimeoutNs;
+    p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs;
+    p.H = H;
+    p.T = T;
+    if (launch_attn_fwd<D, false>(mq, mk, mv, p, dev->sm_count, stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 template <int D, bool F8>
 attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                       const float* dq, const float* dk, const float* dv, int BH, int N, float scale,
@@ -168,6 +223,29 @@ extern "C" attn_status_t attn_fwd_bf16(const void* q, const void* k, const void*
         case 64: return run_fwd<64, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
         case 128: return run_fwd<128, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
         default: return run_fwd<256, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, window, s);
+    }
+}
+
+extern "C" attn_status_t attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, void* o,
+                                              float* lse, const int* cu_seqlens, int num_seqs,
+                                              int max_seqlen, int total_tokens, int H, int d,
+                                              float scale, int causal, int window, void* stream)
+{
+    if (num_seqs < 1 || H < 1 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * H > 0x7fffffffLL || max_seqlen > total_tokens)
+        return ATTN_ERR_INVALID_ARG;
+    if (total_tokens == 0 || max_seqlen == 0) return ATTN_OK;  // nothing to compute
+    if (!q || !k || !v || !o || !lse || !cu_seqlens) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(cu_seqlens, 4))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (d) {
+        case 64: return run_fwd_varlen<64>(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, H, scale, causal, window, s);
+        case 128: return run_fwd_varlen<128>(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, H, scale, causal, window, s);
+        default: return run_fwd_varlen<256>(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, H, scale, causal, window, s);
     }
 }
 

@@ -102,8 +102,10 @@ struct alignas(8) FwdBars {
 };
 
 struct Unit {
-    int bh;      // flattened (batch, head)
-    int q0;      // first query row of the unit
+    int z;       // batched: flattened (batch, head); packed sequences: the head
+    int y0;      // packed sequences: first token of the sequence (0 when batched)
+    int N;       // rows (= keys) of this unit's sequence
+    int q0;      // first query row of the unit, relative to its sequence
     int t0;      // first key tile
     int n;       // key tiles visited
 };
@@ -117,21 +119,40 @@ struct Unit {
 // run at the same time share that head's K/V in L2.  Sub-unit s is half (s & 1)
 // of pair s >> 1, the heavy half first; a CTA walks 2c, 2c+1, 2c+2G, 2c+2G+1, ...
 // Returns false for the empty second half of the middle pair when nq is odd.
+// Packed sequences ("FlashAttention V3：优化框架吞吐量的关键技术实践" §1.1, variable
+// sequence lengths): pair slots are laid out for the longest sequence and a
+// shorter one skips the slots it does not have; offsets are clamped to [0, T] so
+// a unit never addresses a token outside the tensors.
 template <class C>
 __device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w)
 {
     const int npair = (p.num_qblk + 1) >> 1;
     const int pair = s >> 1;
     const int k = pair % npair;
-    w.bh = pair / npair;
-    const int qb = (s & 1) ? k : p.num_qblk - 1 - k;
-    if ((s & 1) && qb == p.num_qblk - 1 - k) return false;
+    int nq = p.num_qblk;
+    if (p.cu_seqlens == nullptr) {
+        w.z = pair / npair;
+        w.y0 = 0;
+        w.N = p.N;
+    } else {
+        const int sh = pair / npair;
+        const int seq = sh / p.H;
+        w.z = sh - seq * p.H;
+        const int a = min(max(__ldg(p.cu_seqlens + seq), 0), p.T);
+        const int b = min(max(__ldg(p.cu_seqlens + seq + 1), a), p.T);
+        w.y0 = a;
+        w.N = b - a;
+        nq = (w.N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+        if (k >= ((nq + 1) >> 1)) return false;  // beyond this sequence's pairs
+    }
+    const int qb = (s & 1) ? k : nq - 1 - k;
+    if ((s & 1) && qb == nq - 1 - k) return false;
     w.q0 = qb * (C::NQ * C::BM);
-    const int r_last = min(p.N, w.q0 + C::NQ * C::BM) - 1;
-    int lo = 0, hi = p.N;  // keys [lo, hi) that some row of the unit may use
+    const int r_last = min(w.N, w.q0 + C::NQ * C::BM) - 1;
+    int lo = 0, hi = w.N;  // keys [lo, hi) that some row of the unit may use
     if (p.window > 0) lo = max(0, w.q0 - p.window);
     if (p.causal) hi = r_last + 1;
-    else if (p.window > 0) hi = min(p.N, r_last + p.window + 1);
+    else if (p.window > 0) hi = min(w.N, r_last + p.window + 1);
     w.t0 = lo / C::BN;
     w.n = (hi + C::BN - 1) / C::BN - w.t0;
     return true;
@@ -238,10 +259,14 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                     mbar_arrive_expect_tx(fb, C::Q_BYTES);
                     ++q_armed[i];
                     const uint32_t dst = smem_u32(q_smem + i * C::Q_BYTES);
+                    const int row = w.q0 + i * C::BM;
 #pragma unroll
-                    for (int cb = 0; cb < C::NCB; ++cb)
-                        tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE,
-                                    w.q0 + i * C::BM, w.bh, pol_q);
+                    for (int cb = 0; cb < C::NCB; ++cb) {
+                        if (p.cu_seqlens == nullptr)  // map (d, N, BH)
+                            tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE, row, w.z, pol_q);
+                        else                          // map (d, H, T)
+                            tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE, w.z, w.y0 + row, pol_q);
+                    }
                 }
                 for (int jj = 0; jj < w.n && ok; ++jj) {
                     const int c0 = (w.t0 + jj) * C::BN;
@@ -259,9 +284,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                         const uint32_t dst = smem_u32(kv_smem + slot * C::KV_BYTES);
                         const CUtensorMap* map = which == 0 ? &tmK : &tmV;
 #pragma unroll
-                        for (int cb = 0; cb < C::NCB; ++cb)
-                            tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, c0,
-                                        w.bh, pol_kv);
+                        for (int cb = 0; cb < C::NCB; ++cb) {
+                            if (p.cu_seqlens == nullptr)
+                                tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, c0, w.z, pol_kv);
+                            else
+                                tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, w.z, w.y0 + c0, pol_kv);
+                        }
                         ++ring;
                     }
                 }
@@ -455,8 +483,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             if (!unit_of<C>(su, p, w)) continue;
             const int a = w.q0 + grp * C::BM;    // first row of this Q tile
             const int row = a + row_in_tile;     // this thread's query row
-            // keys allowed for this row: [jlo, jhi]
-            int jlo = 0, jhi = p.N - 1;
+            // keys allowed for this row: [jlo, jhi] (positions inside the sequence)
+            int jlo = 0, jhi = w.N - 1;
             if (p.causal) jhi = min(jhi, row);
             if (p.window > 0) {
                 jlo = row - p.window;
@@ -465,7 +493,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             // fp8: O is kept in units of the current key tile's V descale: before
             // P(t) V8(t) is added, O *= alpha * dv(t-1) / dv(t).
             float dv_cur = 1.0f, q_desc = 1.0f;
-            if constexpr (F8) q_desc = p.dq[(size_t)w.bh * ((p.N + 127) / 128) + a / 128];
+            if constexpr (F8) q_desc = p.dq[(size_t)w.z * ((p.N + 127) / 128) + a / 128];
 
             int L, R;  // key steps this Q tile needs
             tile_steps<C>(w, grp, p, L, R);
@@ -478,8 +506,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 float dv_ratio = 1.0f;  // fp8: dv(t-1) / dv(t)
                 if constexpr (F8) {
                     const int nkb = (p.N + 127) / 128;
-                    c = p.c_log2 * q_desc * p.dk[(size_t)w.bh * nkb + t];
-                    const float dv_t = p.dv[(size_t)w.bh * nkb + t];
+                    c = p.c_log2 * q_desc * p.dk[(size_t)w.z * nkb + t];
+                    const float dv_t = p.dv[(size_t)w.z * nkb + t];
                     dv_ratio = dv_cur / dv_t;
                     dv_cur = dv_t;
                 }
@@ -498,7 +526,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 float* s = reinterpret_cast<float*>(sr);
 
                 // mask only on tiles that cross a boundary of some row's allowed set
-                const bool edge = (c0 + C::BN > p.N) || (p.causal && c0 + C::BN - 1 > a) ||
+                const bool edge = (c0 + C::BN > w.N) || (p.causal && c0 + C::BN - 1 > a) ||
                                   (p.window > 0 &&
                                    (c0 < a + C::BM - 1 - p.window ||
                                     (!p.causal && c0 + C::BN - 1 > a + p.window)));
@@ -627,8 +655,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
             if constexpr (F8) inv_l *= dv_cur * (1.0f / float(1u << C::P8_SHIFT));
             const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
-            __nv_bfloat16* orow =
-                reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)w.bh * p.N + row) * D;
+            // batched: o[z][row]; packed: o[y0 + row][z] ([T, H, D])
+            const size_t orow_idx = (p.cu_seqlens == nullptr)
+                                        ? (size_t)w.z * p.N + row
+                                        : ((size_t)w.y0 + row) * p.H + w.z;
+            __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + orow_idx * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t r[32];
@@ -639,7 +670,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 for (int e = 0; e < 16; ++e)
                     pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
                                         __uint_as_float(r[2 * e + 1]) * inv_l);
-                if (row < p.N) {
+                if (row < w.N) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -649,9 +680,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[grp]));
-            if (row < p.N) {
+            if (row < w.N) {
                 const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : NEG_INF;
-                p.lse[(size_t)w.bh * p.N + row] = lse2 * 0.69314718055994531f;
+                const size_t li = (p.cu_seqlens == nullptr) ? (size_t)w.z * p.N + row
+                                                            : (size_t)w.z * p.T + w.y0 + row;
+                p.lse[li] = lse2 * 0.69314718055994531f;
             }
             ++uc;
         }

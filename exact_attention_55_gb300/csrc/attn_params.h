@@ -26,6 +26,13 @@ struct FwdParams {
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
     unsigned long long timeout_ns;  // bound on every mbarrier wait
+    // Packed variable-length sequences (null cu_seqlens: the batched [BH, N, D] layout).
+    // q, k, v, o are [T, H, D]; lse is [H, T]; sequence s is tokens [cu[s], cu[s+1]).
+    // Units are (sequence, head, pair of query blocks) with num_qblk from max_seqlen.
+    const int* cu_seqlens;
+    int num_seqs;
+    int H;
+    int T;
 };
 
 struct QuantParams {

@@ -10,6 +10,11 @@ Recipe (one CPU ``torch.Generator`` seeded with ``seed``):
      the outlier entries of Q, K, V (in that order); those entries are
      multiplied by ``mult`` (default 0.1 % of entries, x20).
   3. Each tensor is rounded to bfloat16.  Layout [B, H, N, d], contiguous.
+
+Packed variable-length sequences (``make_packed_qkv``): the same draws with shape
+[T, H, d] (T = sum of the lengths), token-major; ``cu`` holds the offsets.
+``varlen_lengths`` draws a length mix: uniform integers in [lo, hi] from a CPU
+generator, the last length adjusted so the lengths sum to ``total``.
 """
 from __future__ import annotations
 
@@ -68,3 +73,29 @@ def sampled_rows(N: int, count: int, seed: int = 2):
     while len(rows) < min(count, N):
         rows.add(int(torch.randint(0, N, (1,), generator=g).item()))
     return sorted(rows)
+
+
+def make_packed_qkv(lengths, H: int, d: int, seed: int = 0, outliers: bool = False,
+                    frac: float = 1e-3, mult: float = 20.0):
+    """Return bf16 CPU tensors (q, k, v), each [T, H, d], and the int32 offsets cu
+    ([len(lengths) + 1], cu[0] = 0, cu[-1] = T)."""
+    T = int(sum(int(n) for n in lengths))
+    q, k, v = make_qkv(1, 1, T * H, d, seed=seed, outliers=outliers, frac=frac, mult=mult)
+    shape = (T, H, d)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor([int(n) for n in lengths], dtype=torch.int64), 0).to(torch.int32)
+    return q.reshape(shape), k.reshape(shape), v.reshape(shape), cu
+
+
+def varlen_lengths(total: int, lo: int, hi: int, seed: int = 3):
+    """Sequence lengths drawn uniformly from [lo, hi] until they reach ``total``;
+    the last one is cut (or the remainder appended) so the sum is exactly total."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out, acc = [], 0
+    while acc < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g).item())
+        n = min(n, total - acc)
+        out.append(n)
+        acc += n
+    return out

@@ -63,6 +63,32 @@ attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o
                             void* stream);
 
 /*
+ * attn_fwd_bf16_varlen -- attn_fwd_bf16 over variable-length sequences packed
+ * without padding.
+ *
+ * [YT] §1.1 从FlashAttention到V3的迭代路径 (support for variable sequence lengths).
+ * Sequence s is tokens [cu_seqlens[s], cu_seqlens[s+1]); each sequence attends only
+ * within itself, and causal / window masks apply to positions inside it (its first
+ * token is position 0).  Per sequence and head the result is attn_fwd_bf16's.
+ *   q, k, v : const bf16 [T, H, d] (token-major, then head, then d)
+ *   o       : bf16 [T, H, d], written for every token of every sequence
+ *   lse     : float [H, T], written likewise (natural log)
+ *   cu_seqlens : const int32 [num_seqs + 1] in DEVICE memory, non-decreasing from 0
+ *             to total_tokens.  Read on the device only; offsets outside [0, T] are
+ *             clamped there, so a bad table gives wrong results, never a stray access.
+ *   num_seqs >= 1, H >= 1, total_tokens = T >= 0
+ *   max_seqlen : >= the longest sequence and <= T (sizes the work; a longer sequence
+ *             would leave rows unwritten); 0 or T == 0: nothing to do, ATTN_OK (the
+ *             tensor pointers may then be null)
+ *   d in {64, 128, 256}; scale, causal, window as attn_fwd_bf16
+ * Alignment: q, k, v, o 16 bytes; lse, cu_seqlens 4 bytes.
+ */
+attn_status_t attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, const int* cu_seqlens, int num_seqs,
+                                   int max_seqlen, int total_tokens, int H, int d, float scale,
+                                   int causal, int window, void* stream);
+
+/*
  * attn_quantize_fp8_blockwise -- per-block FP8-E4M3 quantisation.
  *
  * [WGC] §3 FP8 量化与精度保持 (per-block dynamic scale onto the FP8 range, whose
