@@ -421,6 +421,25 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
         out["fp8_causal" if causal else "fp8"] = {
             "tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
             "peak": peak8, "peak_source": "fp8 = 2 x measured bf16 burst (nominal ratio)"}
+    # packed variable-length sequences: the same 131072 tokens as lengths uniform in
+    # [512, 16384] (seeded), non-causal and causal; FLOPs over the allowed pairs
+    from exact_attention_55_gb300.inputs import make_packed_qkv, varlen_lengths
+    del q2d, k2d, v2d
+    lengths = varlen_lengths(B * N, 512, 16384, seed=3)
+    qp, kp, vp, cu = make_packed_qkv(lengths, H, D, seed=0)
+    qp, kp, vp, cu = qp.to(dev), kp.to(dev), vp.to(dev), cu.to(dev)
+    op = torch.empty_like(qp)
+    lp = torch.empty((H, qp.shape[0]), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        def varlen_step():
+            fa.attn_fwd_bf16_varlen(qp, kp, vp, cu, max(lengths), scale=scale, causal=causal,
+                                    o=op, lse=lp, stream=stream)
+        ms, per = time_steps(varlen_step, reps, 3, stream)
+        f = sum(4.0 * H * D * allowed_pairs(n, causal, 0) for n in lengths)
+        out["varlen_causal" if causal else "varlen"] = {
+            "tflops": f / (statistics.mean(per) * 1e-3) / 1e12, "ms": statistics.mean(per),
+            "sequences": len(lengths), "tokens": int(sum(lengths)),
+            "lengths": "uniform in [512, 16384], seed 3"}
     status = fa.attn_get_device_status()
     out["device_status"] = status
     return out
