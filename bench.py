@@ -332,7 +332,9 @@ def run_gb300(args, world, rank, local):
         ha = HostAttention(B, H, N, D, chunks=8)
 
         def e2e_step():
-            ha(qh, kh, vh, oh, lh, scale=scale)
+            # inputs are CPU-written pinned buffers, so a step's uploads may overlap the
+            # previous step's last kernel and copies back
+            ha(qh, kh, vh, oh, lh, scale=scale, wait_caller=False)
 
         n_e2e = max(3, min(args.steps, 20))
         barrier(world)
@@ -340,7 +342,8 @@ def run_gb300(args, world, rank, local):
         e2e_ms = max_over_ranks(e2e_ms, world)
         e2e = {"value": world * n_e2e * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": ha.h2d_bytes(), "d2h_bytes_per_step": ha.d2h_bytes(),
-               "steps": n_e2e, "api": "exact_attention_55_gb300.pipeline.HostAttention (8 chunks)"}
+               "steps": n_e2e,
+               "api": "exact_attention_55_gb300.pipeline.HostAttention (8 chunks, steps overlapped)"}
 
     cpu = None
     if rank == 0 and not args.quick:

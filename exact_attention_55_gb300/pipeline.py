@@ -42,6 +42,11 @@ class HostAttention:
         self.s_ins = [torch.cuda.Stream(device=dev) for _ in range(3)]
         self.s_comp = torch.cuda.Stream(device=dev)
         self.s_out = torch.cuda.Stream(device=dev)
+        # buffer-slot state carried across calls: the chunk counter picks the slot, and
+        # the last compute / copy-back that used each slot gates its next reuse
+        self._chunk = 0
+        self._done_comp = [None, None]  # compute finished with slot -> inputs may be overwritten
+        self._done_out = [None, None]   # copy-back finished with slot -> outputs may be overwritten
 
     def h2d_bytes(self) -> int:
         return 3 * self.B * self.H * self.N * self.d * 2
@@ -50,22 +55,30 @@ class HostAttention:
         return self.B * self.H * self.N * (self.d * 2 + 4)
 
     def __call__(self, qh, kh, vh, oh, lseh, scale: float | None = None, causal: bool = False,
-                 window: int = 0) -> None:
+                 window: int = 0, wait_caller: bool = True) -> None:
+        """Enqueue one pass.  With wait_caller (the default) the copies start only after
+        the work already queued on the caller's stream, so inputs written there (for
+        instance the outputs of a previous call) are seen.  With wait_caller=False the
+        inputs must already be in host memory (written by the CPU): the uploads of this
+        call may then overlap the previous call's last kernels and copies back."""
         for n, t in (("q", qh), ("k", kh), ("v", vh), ("o", oh)):
             if t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (
                     self.B, self.H, self.N, self.d):
                 raise TypeError(f"{n} must be a host bf16 tensor of shape {(self.B, self.H, self.N, self.d)}")
+        if lseh.is_cuda or lseh.dtype != torch.float32 or tuple(lseh.shape) != (self.B, self.H, self.N):
+            raise TypeError(f"lse must be a host float32 tensor of shape {(self.B, self.H, self.N)}")
         if scale is None:
             scale = 1.0 / math.sqrt(self.d)
         caller = torch.cuda.current_stream()
-        for st in self.s_ins:
-            st.wait_stream(caller)
+        if wait_caller:
+            for st in self.s_ins:
+                st.wait_stream(caller)
         self.s_out.wait_stream(caller)
-        done_comp = [None, None]  # compute finished with buffer slot -> inputs may be overwritten
-        done_out = [None, None]   # copy-back finished with buffer slot -> outputs may be overwritten
+        done_comp, done_out = self._done_comp, self._done_out
         last = None
         for c in range(self.chunks):
-            slot = c & 1
+            slot = self._chunk & 1
+            self._chunk += 1
             b0, b1 = c * self.bc, (c + 1) * self.bc
             evs_in = []
             for st, dst, src in zip(self.s_ins, (self.qd, self.kd, self.vd), (qh, kh, vh)):

@@ -26,3 +26,27 @@ def test_pipelined_host_call_equals_single_launch(causal, window):
         torch.cuda.synchronize()
         assert fa.attn_get_device_status() == fa.ATTN_OK
         assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, lse_ref.cpu())
+
+
+def test_overlapped_calls_on_changing_inputs():
+    """wait_caller=False with different CPU-written inputs and outputs per call: slot
+    state carried across calls keeps every call's result exact while the next call's
+    uploads overlap the previous call's tail."""
+    require_gpu()
+    import exact_attention_55_gb300 as fa
+    from exact_attention_55_gb300.pipeline import HostAttention
+    B, H, N, d = 4, 4, 1024, 64
+    ha = HostAttention(B, H, N, d, chunks=4)   # 4 chunks per call, 2 slots: parity alternates
+    calls = []
+    for seed in (60, 61, 62):
+        q, k, v = make_qkv(B, H, N, d, seed=seed)
+        ins = [t.pin_memory() for t in (q, k, v)]
+        oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        ha(*ins, oh, lh, causal=True, wait_caller=False)
+        calls.append((q, k, v, oh, lh))
+    torch.cuda.synchronize()
+    assert fa.attn_get_device_status() == fa.ATTN_OK
+    for q, k, v, oh, lh in calls:
+        o_ref, lse_ref = fa.attn_fwd_bf16(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, lse_ref.cpu())
