@@ -29,6 +29,9 @@ Functions and the passage each follows:
   attn_varlen_f64            variable-length sequences packed without padding ([YT]
                              §1.1 可变序列长度): each sequence attends only within
                              itself, masks relative to its own first token
+  attn_decode_paged_f64      a decoding step against a paged KV cache ([JJ] §3 总结:
+                             tokens generated one at a time over cached K/V; [WGC]
+                             §局限性与后续方向 item 2: PagedAttention KV-cache management)
 Every function is pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``.
 """
 from __future__ import annotations
@@ -173,6 +176,42 @@ def attn_varlen_f64(q, k, v, cu_seqlens, scale: float, causal: bool = False, win
                           v[a:b].transpose(1, 0, 2), scale, causal=causal, window=window)
         o[a:b] = oh.transpose(1, 0, 2)
         lse[:, a:b] = lh
+    return o, lse
+
+
+def attn_decode_paged_f64(q, k_cache, v_cache, page_table, seq_lens, scale: float):
+    """One decoding step over a paged KV cache.
+    q: [B, H, nq, d], the nq newest tokens of each sequence; k_cache, v_cache:
+    [num_pages, H, page_size, d]; page_table: [B, max_pages] page numbers in order;
+    seq_lens: [B] cached lengths L_b >= nq (the new tokens' keys included).  Key t of
+    sequence b is row t % page_size of page page_table[b][t // page_size]; query i
+    sits at position L_b - nq + i and sees keys 0 .. L_b - nq + i.
+    Returns (O [B, H, nq, d], LSE [B, H, nq]) float64."""
+    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    pt = np.asarray(page_table, dtype=np.int64)
+    lens = [int(x) for x in np.asarray(seq_lens).reshape(-1)]
+    B, H, nq, d = q.shape
+    ps = kc.shape[2]
+    o = np.zeros((B, H, nq, d))
+    lse = np.zeros((B, H, nq))
+    for b in range(B):
+        L = lens[b]
+        if L < nq:
+            raise ValueError("seq_lens must be >= nq")
+        t = np.arange(L)
+        pages = pt[b, t // ps]
+        rows = t % ps
+        for h in range(H):
+            K = kc[pages, h, rows]          # [L, d], keys in sequence order
+            V = vc[pages, h, rows]
+            s = scale * (q[b, h] @ K.T)     # [nq, L]
+            for i in range(nq):
+                last = L - nq + i           # causal, aligned to the end of the sequence
+                si = s[i, :last + 1]
+                m = si.max()
+                e = np.exp(si - m)
+                o[b, h, i] = (e @ V[:last + 1]) / e.sum()
+                lse[b, h, i] = m + np.log(e.sum())
     return o, lse
 
 
