@@ -12,6 +12,7 @@ raises.
     o8, lse8 = fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv)
     q8h, sqh = fa.attn_quantize_fp8_hadamard(q)              # rotate rows, then quantise (Q, K)
     o, lse = fa.attn_fwd_bf16_varlen(qp, kp, vp, cu, max_len) # packed [T, H, d], int32 offsets
+    o, lse = fa.attn_decode_bf16_paged(q1, kc, vc, table, lens) # decoding step, paged KV cache
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
-    "attn_fwd_bf16_varlen",
+    "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
@@ -40,7 +41,8 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_quantize_fp8_blockwise",
+    "attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_decode_bf16_paged",
+    "attn_decode_workspace_bytes", "attn_quantize_fp8_blockwise",
     "attn_quantize_fp8_hadamard",
     "attn_fwd_fp8", "attn_status_string", "attn_get_device_status",
     "attn_selftest_wait_timeout",
@@ -76,6 +78,11 @@ def load_library(path: str | None = None):
         lib.attn_fwd_bf16.restype = i
         lib.attn_fwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_bf16_varlen.restype = i
+        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
+                                               i, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_bf16_paged.restype = i
         lib.attn_quantize_fp8_blockwise.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.attn_quantize_fp8_blockwise.restype = i
         lib.attn_quantize_fp8_hadamard.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -177,6 +184,57 @@ def attn_fwd_bf16_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: float | No
                                              int(max_seqlen), T, H, d, float(scale),
                                              int(bool(causal)), int(window), _stream_handle(stream))
     _raise_if(st, "attn_fwd_bf16_varlen")
+    return o, lse
+
+
+def attn_decode_workspace_bytes(B: int, H: int, nq: int, d: int, max_pages: int,
+                                num_splits: int = 0) -> int:
+    """Workspace bytes attn_decode_bf16_paged needs for that plan (0: one split)."""
+    return int(load_library().attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits))
+
+
+def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | None = None,
+                           num_splits: int = 0, workspace=None, o=None, lse=None, stream=None):
+    """One decoding step over a paged KV cache.  q: bf16 [B, H, nq, d] (the nq newest
+    tokens, nq <= 8); k_cache, v_cache: bf16 [num_pages, H, page_size, d]; page_table:
+    int32 [B, max_pages]; seq_lens: int32 [B] (cached lengths, the new tokens included).
+    Returns O [B, H, nq, d] and the natural-log LSE [B, H, nq].  A workspace of
+    attn_decode_workspace_bytes(...) is allocated when none is given."""
+    _check_bhnd("q", q, torch.bfloat16)
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_bhnd(n, t, torch.bfloat16)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    B, H, nq, d = q.shape
+    num_pages, Hc, page_size, dc = k_cache.shape
+    if Hc != H or dc != d:
+        raise ValueError("cache heads / head dim must match q")
+    for n, t in (("page_table", page_table), ("seq_lens", seq_lens)):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or t.device != q.device
+                or not t.is_contiguous()):
+            raise TypeError(f"{n} must be a contiguous int32 tensor on q's device")
+    if page_table.dim() != 2 or page_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("page_table must be [B, max_pages] and seq_lens [B]")
+    max_pages = page_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, nq), dtype=torch.float32, device=q.device)
+    _check_out(o, (B, H, nq, d), torch.bfloat16, q.device, "o")
+    _check_out(lse, (B, H, nq), torch.float32, q.device, "lse")
+    if workspace is None:
+        nbytes = attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits)
+        workspace = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    st = load_library().attn_decode_bf16_paged(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
+        seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, nq, d, page_size, num_pages,
+        max_pages, float(scale), int(num_splits), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _raise_if(st, "attn_decode_bf16_paged")
     return o, lse
 
 

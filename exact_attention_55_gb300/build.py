@@ -27,6 +27,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompil
 UNITS = [
     ("api", "api.cu", []),
     ("quant_fp8", "quant_fp8.cu", []),
+    ("decode", "decode.cu", []),
     ("fwd_bf16_d64", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=64", "-DGB300_ATTN_F8=0"]),
     ("fwd_bf16_d128", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=128", "-DGB300_ATTN_F8=0"]),
     ("fwd_bf16_d256", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=256", "-DGB300_ATTN_F8=0"]),

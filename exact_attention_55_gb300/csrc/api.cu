@@ -20,6 +20,7 @@
 namespace gb300 {
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
@@ -201,6 +202,22 @@ attn_status_t check_common(int B, int H, int N, float scale, long long* BH)
     return ATTN_OK;
 }
 
+// Split plan of a decoding step: requested > 0 is taken as is (at most max_pages);
+// 0 picks about four CTAs per SM.  Returns the splits and pages per split.
+void decode_plan(int BH, int max_pages, int requested, int sm_count, int* splits, int* pps)
+{
+    long long want = requested > 0 ? requested : (4LL * sm_count + BH - 1) / BH;
+    if (want < 1) want = 1;
+    if (want > max_pages) want = max_pages;
+    *pps = (int)((max_pages + want - 1) / want);
+    *splits = (max_pages + *pps - 1) / *pps;
+}
+
+size_t decode_ws_bytes(long long BH, int splits, int nq, int d)
+{
+    return splits > 1 ? (size_t)BH * splits * nq * (d + 1) * sizeof(float) : 0;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -350,4 +367,76 @@ extern "C" attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_n
     if (st != ATTN_OK) return st;
     wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, timeout_ns);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int max_pages,
+                                             int num_splits)
+{
+    if (B < 1 || H < 1 || nq < 1 || d < 1 || max_pages < 1) return 0;
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != ATTN_OK) return 0;
+    int splits = 1, pps = 1;
+    decode_plan(B * H, max_pages, num_splits, dev->sm_count, &splits, &pps);
+    return decode_ws_bytes((long long)B * H, splits, nq, d);
+}
+
+extern "C" attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache,
+                                               const void* v_cache, const int* page_table,
+                                               const int* seq_lens, void* o, float* lse, int B,
+                                               int H, int nq, int d, int page_size,
+                                               int num_pages, int max_pages, float scale,
+                                               int num_splits, void* workspace,
+                                               size_t workspace_bytes, void* stream)
+{
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !lse)
+        return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || nq < 1 || num_pages < 1 || max_pages < 1 || num_splits < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    if (nq > 8 || (long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (page_size < 1 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+        return ATTN_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+        (workspace && !aligned(workspace, 16)))
+        return ATTN_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    const long long BH = (long long)B * H;
+    int splits = 1, pps = 1;
+    decode_plan((int)BH, max_pages, num_splits, dev->sm_count, &splits, &pps);
+    if (decode_ws_bytes(BH, splits, nq, d) > (workspace ? workspace_bytes : 0)) {
+        if (num_splits > 0) return ATTN_ERR_INVALID_ARG;   // asked for more than fits
+        // automatic plan: fall back to as many splits as the workspace holds
+        const long long per = BH * nq * (d + 1) * (long long)sizeof(float);
+        const long long fit = workspace ? (long long)(workspace_bytes / per) : 1;
+        decode_plan((int)BH, max_pages, fit > 1 ? (int)fit : 1, dev->sm_count, &splits, &pps);
+    }
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.kc = k_cache;
+    p.vc = v_cache;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.o = o;
+    p.lse = lse;
+    p.ws = static_cast<float*>(workspace);
+    p.B = B;
+    p.H = H;
+    p.nq = nq;
+    int lg = 0;
+    while ((1 << lg) < page_size) ++lg;
+    p.log2_ps = lg;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.splits = splits;
+    p.pages_per_split = pps;
+    p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    if (launch_decode(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }

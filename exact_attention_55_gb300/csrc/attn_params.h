@@ -35,6 +35,23 @@ struct FwdParams {
     int T;
 };
 
+// One decoding step over a paged KV cache (decode.cu).
+struct DecodeParams {
+    const void* q;        // bf16 [B, H, nq, D]
+    const void* kc;       // bf16 [num_pages, H, page_size, D]
+    const void* vc;       // bf16 [num_pages, H, page_size, D]
+    const int* page_table;  // int32 [B, max_pages]
+    const int* seq_lens;  // int32 [B]
+    void* o;              // bf16 [B, H, nq, D]
+    float* lse;           // fp32 [B, H, nq], natural log
+    float* ws;            // fp32 [B*H, splits, nq, D + 1] when splits > 1
+    int B, H, nq;
+    int log2_ps;          // page_size = 1 << log2_ps
+    int num_pages, max_pages;
+    int splits, pages_per_split;
+    float c_log2;         // softmax scale * log2(e)
+};
+
 struct QuantParams {
     const void* x;        // bf16 [BH, N, d]
     uint8_t* x8;          // e4m3 [BH, N, d]

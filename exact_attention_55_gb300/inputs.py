@@ -15,6 +15,12 @@ Packed variable-length sequences (``make_packed_qkv``): the same draws with shap
 [T, H, d] (T = sum of the lengths), token-major; ``cu`` holds the offsets.
 ``varlen_lengths`` draws a length mix: uniform integers in [lo, hi] from a CPU
 generator, the last length adjusted so the lengths sum to ``total``.
+
+Paged KV cache (``make_paged_cache``): one generator draws q ([B, H, nq, d]), then
+the K pool and the V pool ([num_pages, H, page_size, d], num_pages = the pages the
+sequences need plus ``spare``), then a permutation of the pages; sequence b takes
+the next ceil(L_b / page_size) pages of that permutation, in order.  Unused table
+entries are 0.
 """
 from __future__ import annotations
 
@@ -99,3 +105,23 @@ def varlen_lengths(total: int, lo: int, hi: int, seed: int = 3):
         out.append(n)
         acc += n
     return out
+
+
+def make_paged_cache(lens, H: int, nq: int, d: int, page_size: int, seed: int = 0, spare: int = 3):
+    """Return (q, k_cache, v_cache, page_table int32 [B, max_pages], seq_lens int32 [B])."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    B = len(lens)
+    need = [(int(L) + page_size - 1) // page_size for L in lens]
+    max_pages = max(1, max(need))
+    num_pages = sum(need) + spare
+    q = torch.randn((B, H, nq, d), generator=g).to(torch.bfloat16)
+    kc = torch.randn((num_pages, H, page_size, d), generator=g).to(torch.bfloat16)
+    vc = torch.randn((num_pages, H, page_size, d), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(num_pages, generator=g)
+    table = torch.zeros((B, max_pages), dtype=torch.int32)
+    used = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[used:used + n].to(torch.int32)
+        used += n
+    return q, kc, vc, table, torch.tensor([int(L) for L in lens], dtype=torch.int32)

@@ -28,6 +28,8 @@
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -87,6 +89,37 @@ attn_status_t attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, 
                                    float* lse, const int* cu_seqlens, int num_seqs,
                                    int max_seqlen, int total_tokens, int H, int d, float scale,
                                    int causal, int window, void* stream);
+
+/*
+ * attn_decode_bf16_paged -- one decoding step of attention over a paged KV cache.
+ *
+ * [JJ] §3 总结 (decoding produces tokens one at a time over a cache of earlier keys
+ * and values) and [WGC] 局限性与后续方向 item 2 (PagedAttention KV-cache management).
+ * For sequence b with seq_lens[b] = L cached tokens (its nq newest included) and head
+ * h, query i is the token at position L - nq + i and attends to keys 0 .. L - nq + i:
+ *     O = softmax(scale * q K^T) V over those keys, LSE = natural log of the sum.
+ * Key t of sequence b is row t % page_size of page page_table[b][t / page_size].
+ *   q          : const bf16 [B, H, nq, d]; 1 <= nq <= 8
+ *   k_cache, v_cache : const bf16 [num_pages, H, page_size, d]
+ *   page_table : const int32 [B, max_pages] (device); entries are clamped to
+ *                [0, num_pages) on the device, so a bad table never reads outside
+ *   seq_lens   : const int32 [B] (device); clamped to [0, max_pages * page_size];
+ *                rows of a sequence shorter than nq get O = 0, LSE = -inf
+ *   o, lse     : bf16 [B, H, nq, d], float [B, H, nq], written
+ *   d in {64, 128, 256}; page_size a power of two <= 65536; B * H <= 65535
+ *   num_splits : key splits per (sequence, head); 0 picks about four CTAs per SM
+ *   workspace  : device memory of attn_decode_workspace_bytes(...) bytes (16-byte
+ *                aligned; may be NULL when that is 0).  With num_splits = 0 a smaller
+ *                workspace lowers the splits to what fits; with num_splits > 0 it is
+ *                ATTN_ERR_INVALID_ARG.
+ * HBM-bound: the keys and values of every sequence are read once per call.
+ */
+size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int max_pages, int num_splits);
+attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache,
+                                     const int* page_table, const int* seq_lens, void* o,
+                                     float* lse, int B, int H, int nq, int d, int page_size,
+                                     int num_pages, int max_pages, float scale, int num_splits,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_quantize_fp8_blockwise -- per-block FP8-E4M3 quantisation.

@@ -27,9 +27,23 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for n in ("attn_fwd_bf16", "attn_quantize_fp8_blockwise", "attn_fwd_fp8",
-              "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout"):
+    for n in ("attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_decode_bf16_paged",
+              "attn_decode_workspace_bytes", "attn_quantize_fp8_blockwise",
+              "attn_quantize_fp8_hadamard", "attn_fwd_fp8", "attn_status_string",
+              "attn_get_device_status", "attn_selftest_wait_timeout"):
         assert n in names
+
+
+def test_header_is_plain_c():
+    """The boundary header compiles on its own as C (no C++ or CUDA types leak in)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_every_declared_symbol_is_exported(lib):
