@@ -315,10 +315,6 @@ def run_gb300(args, world, rank, local):
                 "peak_source": peak_src + " bf16 burst (cuBLAS 8192^3)",
                 "flops_per_launch": f_step}
 
-    extra = {}
-    if rank == 0 and not args.quick:
-        extra = measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks)
-
     # e2e through the public API with pinned host buffers: HostAttention cuts the
     # batch into chunks and overlaps host->device copies, the kernel and the copies
     # back; every byte of Q/K/V goes up and every byte of O/LSE comes back each step.
@@ -344,6 +340,15 @@ def run_gb300(args, world, rank, local):
                "h2d_bytes_per_step": ha.h2d_bytes(), "d2h_bytes_per_step": ha.d2h_bytes(),
                "steps": n_e2e,
                "api": "exact_attention_55_gb300.pipeline.HostAttention (8 chunks, steps overlapped)"}
+        del ha, qh, kh, vh, oh, lh
+
+    # the other workloads run after the end-to-end leg, whose pinned buffers should be
+    # allocated before these legs' large host-side input generation
+    extra = {}
+    if rank == 0 and not args.quick:
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        extra = measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks)
+        del qd, kd, vd
 
     cpu = None
     if rank == 0 and not args.quick:
@@ -443,6 +448,33 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
             "tflops": f / (statistics.mean(per) * 1e-3) / 1e12, "ms": statistics.mean(per),
             "sequences": len(lengths), "tokens": int(sum(lengths)),
             "lengths": "uniform in [512, 16384], seed 3"}
+    # decoding step over a paged KV cache: B=16 sequences x H=16 heads, 8192 cached
+    # tokens each in 64-token pages, d=128, one new token; HBM-bound (K and V read once)
+    from exact_attention_55_gb300.inputs import make_paged_cache
+    del qp, kp, vp, op, lp
+    dq_, dkc, dvc, dpt, dsl = make_paged_cache([N] * B, H, 1, D, 64, seed=0)
+    dq_, dkc, dvc, dpt, dsl = (t.to(dev) for t in (dq_, dkc, dvc, dpt, dsl))
+    do_ = torch.empty_like(dq_)
+    dl_ = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    nws = fa.attn_decode_workspace_bytes(B, H, 1, D, dpt.shape[1], 0)
+    dws = torch.empty(max(nws // 4, 1), dtype=torch.float32, device=dev)
+
+    def decode_step():
+        fa.attn_decode_bf16_paged(dq_, dkc, dvc, dpt, dsl, scale=scale, workspace=dws, o=do_,
+                                  lse=dl_, stream=stream)
+    ms, per = time_steps(decode_step, reps, 3, stream)
+    dbytes = 2 * B * H * N * D * 2 + 2 * dq_.numel() * 2 + dl_.numel() * 4
+    gbs = dbytes / (statistics.mean(per) * 1e-3) / 1e9
+    out["decode_paged"] = {"GB_per_s": gbs, "frac_of_hbm": gbs / hbm, "us": 1e3 * statistics.mean(per),
+                           "bytes": dbytes, "shape": "B16 H16 L8192 d128 nq1, 64-token pages"}
+
+    def decode_noalloc_step():
+        fa.attn_decode_bf16_paged_noalloc(dq_, dkc, dvc, dpt, dsl, scale=scale, o=do_, lse=dl_,
+                                          stream=stream)
+    ms, per = time_steps(decode_noalloc_step, reps, 3, stream)
+    gbs = dbytes / (statistics.mean(per) * 1e-3) / 1e9
+    out["decode_paged_noalloc"] = {"GB_per_s": gbs, "frac_of_hbm": gbs / hbm,
+                                   "us": 1e3 * statistics.mean(per)}
     status = fa.attn_get_device_status()
     out["device_status"] = status
     return out
@@ -472,6 +504,12 @@ def run_profile_case(args):
     elif args.profile == "quant_hadamard":
         def run():
             fa.attn_quantize_fp8_hadamard(qd)
+    elif args.profile == "decode":
+        from exact_attention_55_gb300.inputs import make_paged_cache
+        dq_, dkc, dvc, dpt, dsl = (t.cuda() for t in make_paged_cache([n] * 8, h, 1, d, 64, seed=0))
+
+        def run():
+            fa.attn_decode_bf16_paged(dq_, dkc, dvc, dpt, dsl, scale=scale)
     else:
         qs = [fa.attn_quantize_fp8_blockwise(t) for t in (qd, kd, vd)]
 
@@ -549,7 +587,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
     ap.add_argument("--profile", default=None,
                     choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant",
-                             "quant_hadamard"],
+                             "quant_hadamard", "decode"],
                     help="run a small case of one kernel (for ncu) and exit")
     ap.add_argument("--sweep", action="store_true",
                     help="time the d x N x mask sweep (one JSON line per point) and exit")

@@ -27,7 +27,8 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
-    "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_workspace_bytes",
+    "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_bf16_paged_noalloc",
+    "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
@@ -42,7 +43,8 @@ ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
     "attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_decode_bf16_paged",
-    "attn_decode_workspace_bytes", "attn_quantize_fp8_blockwise",
+    "attn_decode_bf16_paged_noalloc", "attn_decode_workspace_bytes",
+    "attn_quantize_fp8_blockwise",
     "attn_quantize_fp8_hadamard",
     "attn_fwd_fp8", "attn_status_string", "attn_get_device_status",
     "attn_selftest_wait_timeout",
@@ -83,6 +85,9 @@ def load_library(path: str | None = None):
         lib.attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
                                                i, vp, ctypes.c_size_t, vp]
         lib.attn_decode_bf16_paged.restype = i
+        lib.attn_decode_bf16_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                                       i, i, f, i, vp]
+        lib.attn_decode_bf16_paged_noalloc.restype = i
         lib.attn_quantize_fp8_blockwise.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.attn_quantize_fp8_blockwise.restype = i
         lib.attn_quantize_fp8_hadamard.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
@@ -193,13 +198,7 @@ def attn_decode_workspace_bytes(B: int, H: int, nq: int, d: int, max_pages: int,
     return int(load_library().attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits))
 
 
-def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | None = None,
-                           num_splits: int = 0, workspace=None, o=None, lse=None, stream=None):
-    """One decoding step over a paged KV cache.  q: bf16 [B, H, nq, d] (the nq newest
-    tokens, nq <= 8); k_cache, v_cache: bf16 [num_pages, H, page_size, d]; page_table:
-    int32 [B, max_pages]; seq_lens: int32 [B] (cached lengths, the new tokens included).
-    Returns O [B, H, nq, d] and the natural-log LSE [B, H, nq].  A workspace of
-    attn_decode_workspace_bytes(...) is allocated when none is given."""
+def _decode_args(q, k_cache, v_cache, page_table, seq_lens, scale, o, lse):
     _check_bhnd("q", q, torch.bfloat16)
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache)):
         _check_bhnd(n, t, torch.bfloat16)
@@ -224,6 +223,18 @@ def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: flo
         lse = torch.empty((B, H, nq), dtype=torch.float32, device=q.device)
     _check_out(o, (B, H, nq, d), torch.bfloat16, q.device, "o")
     _check_out(lse, (B, H, nq), torch.float32, q.device, "lse")
+    return B, H, nq, d, num_pages, page_size, max_pages, scale, o, lse
+
+
+def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | None = None,
+                           num_splits: int = 0, workspace=None, o=None, lse=None, stream=None):
+    """One decoding step over a paged KV cache.  q: bf16 [B, H, nq, d] (the nq newest
+    tokens, nq <= 8); k_cache, v_cache: bf16 [num_pages, H, page_size, d]; page_table:
+    int32 [B, max_pages]; seq_lens: int32 [B] (cached lengths, the new tokens included).
+    Returns O [B, H, nq, d] and the natural-log LSE [B, H, nq].  A workspace of
+    attn_decode_workspace_bytes(...) is allocated when none is given."""
+    B, H, nq, d, num_pages, page_size, max_pages, scale, o, lse = _decode_args(
+        q, k_cache, v_cache, page_table, seq_lens, scale, o, lse)
     if workspace is None:
         nbytes = attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits)
         workspace = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
@@ -235,6 +246,21 @@ def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: flo
         max_pages, float(scale), int(num_splits), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _raise_if(st, "attn_decode_bf16_paged")
+    return o, lse
+
+
+def attn_decode_bf16_paged_noalloc(q, k_cache, v_cache, page_table, seq_lens,
+                                   scale: float | None = None, num_splits: int = 0, o=None,
+                                   lse=None, stream=None):
+    """attn_decode_bf16_paged with the split partials in the library's own device
+    scratch (no workspace); calls on one device must be ordered."""
+    B, H, nq, d, num_pages, page_size, max_pages, scale, o, lse = _decode_args(
+        q, k_cache, v_cache, page_table, seq_lens, scale, o, lse)
+    st = load_library().attn_decode_bf16_paged_noalloc(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
+        seq_lens.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, nq, d, page_size, num_pages,
+        max_pages, float(scale), int(num_splits), _stream_handle(stream))
+    _raise_if(st, "attn_decode_bf16_paged_noalloc")
     return o, lse
 
 

@@ -25,6 +25,11 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
 
+// Device-wide scratch for attn_decode_bf16_paged_noalloc: the split partials of a
+// decoding step live here instead of in a caller-provided workspace.  16 MB.
+constexpr size_t kDecodeScratchFloats = size_t(1) << 22;
+static __device__ __align__(256) float g_decode_scratch[kDecodeScratchFloats];
+
 // A bounded wait on a barrier that no thread arrives on: exercises the timeout
 // path (give up, record the status, return) without faulting or hanging.
 __global__ void wait_timeout_kernel(int* status, unsigned long long timeout_ns)
@@ -46,6 +51,7 @@ struct DeviceInfo {
     bool ready = false;
     int sm_count = 0;
     int* status = nullptr;
+    float* decode_scratch = nullptr;
 };
 
 std::mutex g_mutex;
@@ -65,8 +71,11 @@ attn_status_t device_info(DeviceInfo** out)
             return ATTN_ERR_CUDA;
         void* addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
+        void* scratch = nullptr;
+        if (cudaGetSymbolAddress(&scratch, g_decode_scratch) != cudaSuccess) return ATTN_ERR_CUDA;
         d.sm_count = sms;
         d.status = static_cast<int*>(addr);
+        d.decode_scratch = static_cast<float*>(scratch);
         d.ready = true;
     }
     if (g_encode == nullptr) {
@@ -380,13 +389,11 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int m
     return decode_ws_bytes((long long)B * H, splits, nq, d);
 }
 
-extern "C" attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache,
-                                               const void* v_cache, const int* page_table,
-                                               const int* seq_lens, void* o, float* lse, int B,
-                                               int H, int nq, int d, int page_size,
-                                               int num_pages, int max_pages, float scale,
-                                               int num_splits, void* workspace,
-                                               size_t workspace_bytes, void* stream)
+static attn_status_t decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                  const int* page_table, const int* seq_lens, void* o, float* lse,
+                                  int B, int H, int nq, int d, int page_size, int num_pages,
+                                  int max_pages, float scale, int num_splits, void* workspace,
+                                  size_t workspace_bytes, bool use_scratch, void* stream)
 {
     if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !lse)
         return ATTN_ERR_INVALID_ARG;
@@ -405,6 +412,10 @@ extern "C" attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cac
     DeviceInfo* dev = nullptr;
     attn_status_t st = device_info(&dev);
     if (st != ATTN_OK) return st;
+    if (use_scratch) {
+        workspace = dev->decode_scratch;
+        workspace_bytes = kDecodeScratchFloats * sizeof(float);
+    }
     const long long BH = (long long)B * H;
     int splits = 1, pps = 1;
     decode_plan((int)BH, max_pages, num_splits, dev->sm_count, &splits, &pps);
@@ -439,4 +450,29 @@ extern "C" attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cac
     if (launch_decode(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache,
+                                               const void* v_cache, const int* page_table,
+                                               const int* seq_lens, void* o, float* lse, int B,
+                                               int H, int nq, int d, int page_size,
+                                               int num_pages, int max_pages, float scale,
+                                               int num_splits, void* workspace,
+                                               size_t workspace_bytes, void* stream)
+{
+    return decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, H, nq, d, page_size,
+                        num_pages, max_pages, scale, num_splits, workspace, workspace_bytes, false,
+                        stream);
+}
+
+extern "C" attn_status_t attn_decode_bf16_paged_noalloc(const void* q, const void* k_cache,
+                                                       const void* v_cache,
+                                                       const int* page_table,
+                                                       const int* seq_lens, void* o, float* lse,
+                                                       int B, int H, int nq, int d, int page_size,
+                                                       int num_pages, int max_pages, float scale,
+                                                       int num_splits, void* stream)
+{
+    return decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, H, nq, d, page_size,
+                        num_pages, max_pages, scale, num_splits, nullptr, 0, true, stream);
 }

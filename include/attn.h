@@ -122,6 +122,23 @@ attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache, const v
                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_bf16_paged_noalloc -- attn_decode_bf16_paged without a caller workspace.
+ *
+ * The split partials go to one 16 MB scratch array of the library on each device
+ * (a file-scope static device array), so the call needs no memory from the caller.
+ * With num_splits = 0 the plan shrinks to what the scratch holds; num_splits > 0
+ * that does not fit is ATTN_ERR_INVALID_ARG.  The scratch is shared: calls through
+ * this entry point on one device must be ordered (one stream, or streams the caller
+ * synchronises); attn_decode_bf16_paged with a workspace per stream has no such rule.
+ */
+attn_status_t attn_decode_bf16_paged_noalloc(const void* q, const void* k_cache,
+                                             const void* v_cache, const int* page_table,
+                                             const int* seq_lens, void* o, float* lse, int B,
+                                             int H, int nq, int d, int page_size, int num_pages,
+                                             int max_pages, float scale, int num_splits,
+                                             void* stream);
+
+/*
  * attn_quantize_fp8_blockwise -- per-block FP8-E4M3 quantisation.
  *
  * [WGC] §3 FP8 量化与精度保持 (per-block dynamic scale onto the FP8 range, whose
