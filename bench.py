@@ -456,7 +456,7 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     dq_, dkc, dvc, dpt, dsl = (t.to(dev) for t in (dq_, dkc, dvc, dpt, dsl))
     do_ = torch.empty_like(dq_)
     dl_ = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
-    nws = fa.attn_decode_workspace_bytes(B, H, 1, D, dpt.shape[1], 0)
+    nws = fa.attn_decode_workspace_bytes(B, H, 1, D, 64, dpt.shape[1], 0)
     dws = torch.empty(max(nws // 4, 1), dtype=torch.float32, device=dev)
 
     def decode_step():

@@ -80,7 +80,7 @@ def load_library(path: str | None = None):
         lib.attn_fwd_bf16.restype = i
         lib.attn_fwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_bf16_varlen.restype = i
-        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
                                                i, vp, ctypes.c_size_t, vp]
@@ -192,10 +192,11 @@ def attn_fwd_bf16_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: float | No
     return o, lse
 
 
-def attn_decode_workspace_bytes(B: int, H: int, nq: int, d: int, max_pages: int,
+def attn_decode_workspace_bytes(B: int, H: int, nq: int, d: int, page_size: int, max_pages: int,
                                 num_splits: int = 0) -> int:
     """Workspace bytes attn_decode_bf16_paged needs for that plan (0: one split)."""
-    return int(load_library().attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits))
+    return int(load_library().attn_decode_workspace_bytes(B, H, nq, d, page_size, max_pages,
+                                                          num_splits))
 
 
 def _decode_args(q, k_cache, v_cache, page_table, seq_lens, scale, o, lse):
@@ -236,7 +237,7 @@ def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: flo
     B, H, nq, d, num_pages, page_size, max_pages, scale, o, lse = _decode_args(
         q, k_cache, v_cache, page_table, seq_lens, scale, o, lse)
     if workspace is None:
-        nbytes = attn_decode_workspace_bytes(B, H, nq, d, max_pages, num_splits)
+        nbytes = attn_decode_workspace_bytes(B, H, nq, d, page_size, max_pages, num_splits)
         workspace = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
     elif not workspace.is_cuda or not workspace.is_contiguous():
         raise TypeError("workspace must be a contiguous CUDA tensor")

@@ -211,15 +211,29 @@ attn_status_t check_common(int B, int H, int N, float scale, long long* BH)
     return ATTN_OK;
 }
 
-// Split plan of a decoding step: requested > 0 is taken as is (at most max_pages);
-// 0 picks about four CTAs per SM.  Returns the splits and pages per split.
-void decode_plan(int BH, int max_pages, int requested, int sm_count, int* splits, int* pps)
+// Split plan of a decoding step: requested > 0 is taken as is (at most max_pages).
+// 0 aims at about 24 four-warp CTAs per SM -- enough loads in flight to keep HBM busy
+// -- but keeps at least 512 keys per split, so the per-split start, merge and the
+// combine stay small against the streaming (measured on B16 H16 L8192 and
+// B1 H16 L65536 decode steps).  Returns the splits and pages per split.
+void decode_plan(int BH, int max_pages, int log2_ps, int requested, int sm_count, int* splits,
+                 int* pps)
 {
-    long long want = requested > 0 ? requested : (4LL * sm_count + BH - 1) / BH;
+    long long want = (24LL * sm_count + BH - 1) / BH;
+    const long long keys_cap = ((long long)max_pages << log2_ps) / 512;
+    if (want > keys_cap) want = keys_cap;
+    if (requested > 0) want = requested;
     if (want < 1) want = 1;
     if (want > max_pages) want = max_pages;
     *pps = (int)((max_pages + want - 1) / want);
     *splits = (max_pages + *pps - 1) / *pps;
+}
+
+int page_log2(int page_size)
+{
+    int lg = 0;
+    while ((1 << lg) < page_size) ++lg;
+    return lg;
 }
 
 size_t decode_ws_bytes(long long BH, int splits, int nq, int d)
@@ -378,14 +392,14 @@ extern "C" attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_n
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int max_pages,
-                                             int num_splits)
+extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int page_size,
+                                             int max_pages, int num_splits)
 {
-    if (B < 1 || H < 1 || nq < 1 || d < 1 || max_pages < 1) return 0;
+    if (B < 1 || H < 1 || nq < 1 || d < 1 || max_pages < 1 || page_size < 1) return 0;
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != ATTN_OK) return 0;
     int splits = 1, pps = 1;
-    decode_plan(B * H, max_pages, num_splits, dev->sm_count, &splits, &pps);
+    decode_plan(B * H, max_pages, page_log2(page_size), num_splits, dev->sm_count, &splits, &pps);
     return decode_ws_bytes((long long)B * H, splits, nq, d);
 }
 
@@ -417,14 +431,15 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
         workspace_bytes = kDecodeScratchFloats * sizeof(float);
     }
     const long long BH = (long long)B * H;
+    const int lg = page_log2(page_size);
     int splits = 1, pps = 1;
-    decode_plan((int)BH, max_pages, num_splits, dev->sm_count, &splits, &pps);
+    decode_plan((int)BH, max_pages, lg, num_splits, dev->sm_count, &splits, &pps);
     if (decode_ws_bytes(BH, splits, nq, d) > (workspace ? workspace_bytes : 0)) {
         if (num_splits > 0) return ATTN_ERR_INVALID_ARG;   // asked for more than fits
         // automatic plan: fall back to as many splits as the workspace holds
         const long long per = BH * nq * (d + 1) * (long long)sizeof(float);
         const long long fit = workspace ? (long long)(workspace_bytes / per) : 1;
-        decode_plan((int)BH, max_pages, fit > 1 ? (int)fit : 1, dev->sm_count, &splits, &pps);
+        decode_plan((int)BH, max_pages, lg, fit > 1 ? (int)fit : 1, dev->sm_count, &splits, &pps);
     }
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
@@ -439,8 +454,6 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     p.B = B;
     p.H = H;
     p.nq = nq;
-    int lg = 0;
-    while ((1 << lg) < page_size) ++lg;
     p.log2_ps = lg;
     p.num_pages = num_pages;
     p.max_pages = max_pages;

@@ -107,14 +107,15 @@ attn_status_t attn_fwd_bf16_varlen(const void* q, const void* k, const void* v, 
  *                rows of a sequence shorter than nq get O = 0, LSE = -inf
  *   o, lse     : bf16 [B, H, nq, d], float [B, H, nq], written
  *   d in {64, 128, 256}; page_size a power of two <= 65536; B * H <= 65535
- *   num_splits : key splits per (sequence, head); 0 picks about four CTAs per SM
+ *   num_splits : key splits per (sequence, head); 0 picks about sixteen CTAs per SM
  *   workspace  : device memory of attn_decode_workspace_bytes(...) bytes (16-byte
  *                aligned; may be NULL when that is 0).  With num_splits = 0 a smaller
  *                workspace lowers the splits to what fits; with num_splits > 0 it is
  *                ATTN_ERR_INVALID_ARG.
  * HBM-bound: the keys and values of every sequence are read once per call.
  */
-size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int max_pages, int num_splits);
+size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int page_size, int max_pages,
+                                   int num_splits);
 attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache, const void* v_cache,
                                      const int* page_table, const int* seq_lens, void* o,
                                      float* lse, int B, int H, int nq, int d, int page_size,

@@ -56,7 +56,7 @@ def test_workspace_rules(fa):
     lens = [4096, 4096]
     q, kc, vc, pt, sl = make_paged_cache(lens, 2, 1, 128, 64, seed=82)
     args = [t.cuda() for t in (q, kc, vc, pt, sl)]
-    need = fa.attn_decode_workspace_bytes(2, 2, 1, 128, pt.shape[1], 8)
+    need = fa.attn_decode_workspace_bytes(2, 2, 1, 128, 64, pt.shape[1], 8)
     assert need == 2 * 2 * 8 * 1 * 129 * 4
     small = torch.empty(16, dtype=torch.float32, device="cuda")
     with pytest.raises(fa.AttnError):          # forced splits that do not fit
