@@ -102,20 +102,38 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const Deco
         for (int e = 0; e < E; ++e) acc[i][e] = 0.0f;
     }
 
+    // groups start at multiples of kDecG inside a split that starts on a page, so with
+    // pages of at least kDecG keys a group never crosses a page
+    const bool group_in_page = p.log2_ps >= 3;
     for (int t0 = k_begin + warp * kDecG; t0 < k_end; t0 += kDecWarps * kDecG) {
+        // edge groups: the split's or the sequence's end falls inside (needs masks)
+        const bool edge = (t0 + kDecG > k_end) || (t0 + kDecG - 1 > L - nq);
         V kr[kDecG], vr[kDecG];
+        if (group_in_page && !edge) {
+            int page = __ldg(ptab + (t0 >> p.log2_ps));
+            page = min(max(page, 0), p.num_pages - 1);
+            const size_t row0 = (((size_t)page * p.H + h) << p.log2_ps) + (t0 & ps_mask);
+            const __nv_bfloat16* kp = kc + row0 * D + lane * E;
+            const __nv_bfloat16* vp = vc + row0 * D + lane * E;
 #pragma unroll
-        for (int g = 0; g < kDecG; ++g) {
-            const int t = t0 + g;
-            if (t < k_end) {
-                int page = __ldg(ptab + (t >> p.log2_ps));
-                page = min(max(page, 0), p.num_pages - 1);
-                const size_t row = (((size_t)page * p.H + h) << p.log2_ps) + (t & ps_mask);
-                kr[g] = load_row<E>(kc + row * D + lane * E);
-                vr[g] = load_row<E>(vc + row * D + lane * E);
-            } else {
-                kr[g] = V{};
-                vr[g] = V{};
+            for (int g = 0; g < kDecG; ++g) {
+                kr[g] = load_row<E>(kp + g * D);
+                vr[g] = load_row<E>(vp + g * D);
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < kDecG; ++g) {
+                const int t = t0 + g;
+                if (t < k_end) {
+                    int page = __ldg(ptab + (t >> p.log2_ps));
+                    page = min(max(page, 0), p.num_pages - 1);
+                    const size_t row = (((size_t)page * p.H + h) << p.log2_ps) + (t & ps_mask);
+                    kr[g] = load_row<E>(kc + row * D + lane * E);
+                    vr[g] = load_row<E>(vc + row * D + lane * E);
+                } else {
+                    kr[g] = V{};
+                    vr[g] = V{};
+                }
             }
         }
         // scores in log2 units: s[g][i] = c * q_i . k_t
@@ -138,13 +156,14 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const Deco
             for (int g = 0; g < kDecG; ++g)
 #pragma unroll
                 for (int i = 0; i < NQ; ++i) s[g][i] += __shfl_xor_sync(0xffffffffu, s[g][i], off);
-        // mask: keys past this split's range, and the end-aligned causal limit
+        // mask: query slots past nq, keys past this split's range, and the end-aligned
+        // causal limit (the last two only in edge groups)
 #pragma unroll
         for (int g = 0; g < kDecG; ++g)
 #pragma unroll
             for (int i = 0; i < NQ; ++i) {
                 const int t = t0 + g;
-                if (i >= nq || t >= k_end || t > L - nq + i) s[g][i] = NEG_INF;
+                if (i >= nq || (edge && (t >= k_end || t > L - nq + i))) s[g][i] = NEG_INF;
             }
         // online softmax: new maxima and rescaling first, then the scores become weights
 #pragma unroll
