@@ -55,6 +55,43 @@ __device__ __forceinline__ typename RowVec<E>::T load_row(const __nv_bfloat16* p
     return __ldcs(reinterpret_cast<const typename RowVec<E>::T*>(p));
 }
 
+// Sum each of the NV values over the 32 lanes and give every lane every sum.  A
+// reduce-scatter first (at each shuffle distance a lane keeps half of its values and
+// adds the partner's copy of that half, while more than one value is left), then a
+// butterfly on the last value, then one broadcast shuffle per value: NV=8 takes 17
+// shuffles instead of 40, and all lanes see bit-identical sums.
+template <int NV>
+__device__ __forceinline__ void warp_sum_all(float* v, int lane)
+{
+    float cur[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) cur[j] = v[j];
+    int c = NV;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        if (c > 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < NV / 2; ++j) {
+                if (j < c / 2) {
+                    const float send = upper ? cur[j] : cur[j + c / 2];
+                    const float keep = upper ? cur[j + c / 2] : cur[j];
+                    cur[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            c >>= 1;
+        } else {
+            cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], o);
+        }
+    }
+    // value idx now sits in slot idx % SLOTS of lane (idx / SLOTS) * (32 / GROUPS)
+    constexpr int SLOTS = NV > 32 ? NV / 32 : 1;
+    constexpr int GROUPS = NV / SLOTS;
+#pragma unroll
+    for (int idx = 0; idx < NV; ++idx)
+        v[idx] = __shfl_sync(0xffffffffu, cur[idx % SLOTS], (idx / SLOTS) * (32 / GROUPS));
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const DecodeParams p)
 {
@@ -150,12 +187,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_split_kernel(const Deco
                 s[g][i] = a;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int g = 0; g < kDecG; ++g)
-#pragma unroll
-                for (int i = 0; i < NQ; ++i) s[g][i] += __shfl_xor_sync(0xffffffffu, s[g][i], off);
+        warp_sum_all<kDecG * NQ>(&s[0][0], lane);
         // mask: query slots past nq, keys past this split's range, and the end-aligned
         // causal limit (the last two only in edge groups)
 #pragma unroll
