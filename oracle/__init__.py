@@ -29,6 +29,9 @@ Functions and the passage each follows:
   attn_varlen_f64            variable-length sequences packed without padding ([YT]
                              §1.1 可变序列长度): each sequence attends only within
                              itself, masks relative to its own first token
+  attn_bwd_f64               gradients of the forward pass (the backward pass the pages
+                             list as the next step after the forward, [YT] §1.1 and
+                             [JJ] §2.3 "forward pass"): dQ, dK, dV of sum(dO * O)
   attn_decode_paged_f64      a decoding step against a paged KV cache ([JJ] §3 总结:
                              tokens generated one at a time over cached K/V; [WGC]
                              §局限性与后续方向 item 2: PagedAttention KV-cache management)
@@ -177,6 +180,37 @@ def attn_varlen_f64(q, k, v, cu_seqlens, scale: float, causal: bool = False, win
         o[a:b] = oh.transpose(1, 0, 2)
         lse[:, a:b] = lh
     return o, lse
+
+
+def attn_bwd_f64(q, k, v, do, scale: float, causal: bool = False, window: int = 0):
+    """Gradients of O = softmax(scale * Q K^T + mask) V for the upstream gradient dO.
+    q, k, v, do: [..., N, d].  With P the masked softmax (two-pass, as attn_f64):
+        dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij (= dO_i . O_i),
+        dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+    Returns (dQ, dK, dV) float64, shaped like q."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    N = q.shape[-2]
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    allowed = np.ones((N, N), dtype=bool)
+    if causal:
+        allowed &= j <= i
+    if window > 0:
+        allowed &= j >= i - window
+        if not causal:
+            allowed &= j <= i + window
+    s = scale * (q @ np.swapaxes(k, -1, -2))
+    s = np.where(allowed, s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.where(allowed, np.exp(s - m), 0.0)
+    p = e / e.sum(axis=-1, keepdims=True)
+    dv = np.swapaxes(p, -1, -2) @ do
+    dp = do @ np.swapaxes(v, -1, -2)
+    dd = (p * dp).sum(axis=-1, keepdims=True)
+    ds = p * (dp - dd)
+    dq = scale * (ds @ k)
+    dk = scale * (np.swapaxes(ds, -1, -2) @ q)
+    return dq, dk, dv
 
 
 def attn_decode_paged_f64(q, k_cache, v_cache, page_table, seq_lens, scale: float):
