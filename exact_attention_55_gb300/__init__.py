@@ -27,6 +27,7 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
+    "attn_bwd_bf16", "attn_bwd_workspace_bytes",
     "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_bf16_paged_noalloc",
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
@@ -42,7 +43,8 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd_bf16", "attn_fwd_bf16_varlen", "attn_decode_bf16_paged",
+    "attn_fwd_bf16", "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_fwd_bf16_varlen",
+    "attn_decode_bf16_paged",
     "attn_decode_bf16_paged_noalloc", "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise",
     "attn_quantize_fp8_hadamard",
@@ -80,6 +82,11 @@ def load_library(path: str | None = None):
         lib.attn_fwd_bf16.restype = i
         lib.attn_fwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_bf16_varlen.restype = i
+        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_bf16.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i,
+                                      i, i, f, i, i, vp]
+        lib.attn_bwd_bf16.restype = i
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
@@ -156,6 +163,41 @@ def attn_fwd_bf16(q, k, v, scale: float | None = None, causal: bool = False, win
                                       int(window), _stream_handle(stream))
     _raise_if(st, "attn_fwd_bf16")
     return o, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    """Workspace bytes attn_bwd_bf16 needs (the per-row D = dO . O)."""
+    return int(load_library().attn_bwd_workspace_bytes(B, H, N))
+
+
+def attn_bwd_bf16(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False,
+                  window: int = 0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass: returns (dQ, dK, dV) bf16 [B, H, N, d] for the upstream gradient dout,
+    given the forward's o and lse (same scale / mask)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_bhnd(n, t, torch.bfloat16)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have q's shape")
+    B, H, N, d = q.shape
+    _check_out(lse, (B, H, N), torch.float32, q.device, "lse")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_out(t, (B, H, N, d), torch.bfloat16, q.device, n)
+    if workspace is None:
+        workspace = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    st = load_library().attn_bwd_bf16(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+        int(bool(causal)), int(window), _stream_handle(stream))
+    _raise_if(st, "attn_bwd_bf16")
+    return dq, dk, dv
 
 
 def attn_fwd_bf16_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,

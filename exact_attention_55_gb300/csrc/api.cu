@@ -21,6 +21,9 @@ namespace gb300 {
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mdo, const BwdParams& p, int d, int sm_count,
+                       cudaStream_t stream);
 
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
@@ -488,4 +491,60 @@ extern "C" attn_status_t attn_decode_bf16_paged_noalloc(const void* q, const voi
 {
     return decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, H, nq, d, page_size,
                         num_pages, max_pages, scale, num_splits, nullptr, 0, true, stream);
+}
+
+extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N)
+{
+    if (B < 1 || H < 1 || N < 1) return 0;
+    return (size_t)B * H * N * sizeof(float);
+}
+
+extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
+                                      const void* dout, const float* lse, void* dq, void* dk,
+                                      void* dv, void* workspace, size_t workspace_bytes, int B,
+                                      int H, int N, int d, float scale, int causal, int window,
+                                      void* stream)
+{
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return ATTN_ERR_INVALID_ARG;
+    long long BH = 0;
+    attn_status_t st = check_common(B, H, N, scale, &BH);
+    if (st != ATTN_OK) return st;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < (size_t)BH * N * sizeof(float)) return ATTN_ERR_INVALID_ARG;
+    const long long nt = (N + 127) / 128;
+    if (BH * nt > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 4))
+        return ATTN_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    alignas(64) CUtensorMap mq, mk, mv, mdo;
+    if (!encode_3d(&mq, q, dt, 2, d, N, (int)BH, 128) || !encode_3d(&mk, k, dt, 2, d, N, (int)BH, 128) ||
+        !encode_3d(&mv, v, dt, 2, d, N, (int)BH, 128) || !encode_3d(&mdo, dout, dt, 2, d, N, (int)BH, 128))
+        return ATTN_ERR_CUDA;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.delta = static_cast<float*>(workspace);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = dev->status;
+    p.BH = (int)BH;
+    p.N = N;
+    p.nt = (int)nt;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    p.scale = scale;
+    p.timeout_ns = kWaitTimeoutNs;
+    if (launch_bwd(mq, mk, mv, mdo, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }

@@ -1,0 +1,442 @@
+// attn_bwd.cu -- backward pass of the fused exact attention: dQ, dK, dV.
+//
+// The gradients of O = softmax(scale * Q K^T + mask) V for an upstream gradient dO,
+// with P recomputed from the forward's per-row log-sum-exp (P = exp(s - LSE), already
+// normalised):
+//     D_i = dO_i . O_i,   dP = dO V^T,   dS = P * (dP - D),
+//     dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO.
+// The pages name the backward pass only as what follows the forward ("FlashAttention
+// V3：优化框架吞吐量的关键技术实践" §1.1; "大模型加速-核心网络算子-Flash Attention V3"
+// §2.3 speaks of the forward pass); the formulas are the chain rule through the
+// forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
+//   bwd_dot_kernel   D_i, one warp per row;
+//   bwd_dq_kernel    per 128-row query tile: S = Q K_j^T and dP = dO V_j^T into TMEM,
+//                    the compute warpgroup turns them into dS (bf16, over S), then
+//                    dQ += dS K_j; K_j serves as the MN-major operand of the last MMA;
+//   bwd_dkdv_kernel  per 128-key tile, the transposed products: S^T = K Q_i^T and
+//                    dP^T = V dO_i^T, then dV += P^T dO_i and dK += dS^T Q_i.
+// S is recomputed in both passes (7 matmuls per tile pair instead of 5) to keep dQ in
+// TMEM rather than in a global fp32 buffer updated by atomics.
+//
+// Roles per CTA (persistent over units): warps 0-3 compute (one thread per row of the
+// tile), warp 4 streams tiles with TMA through an mbarrier ring, warp 5 issues the
+// tcgen05.mma.  Every wait is bounded and gives up with ATTN_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_params.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+template <int D>
+struct BwdCfg {
+    static constexpr int BT = 128;                 // rows of a query or key tile
+    static constexpr int NCB = D / 64;             // 128-byte column blocks of a bf16 row
+    static constexpr int CB_BYTES = BT * 128;
+    static constexpr int TILE_BYTES = NCB * CB_BYTES;
+    static constexpr int SMEM_CAP = 227 * 1024;
+    static constexpr int BAR_BYTES = 1024;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * TILE_BYTES) / TILE_BYTES;
+    static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
+    static constexpr int SMEM_BYTES = ALIGN_SLACK + (2 + NSLOT) * TILE_BYTES + BAR_BYTES;
+    static constexpr int S_COL = 0;      // S (then dS or P) of the step
+    static constexpr int DP_COL = 128;   // dP (then dS^T in the dK/dV pass)
+    static constexpr int ACC_COL = 256;  // dQ, or dV then dK at ACC_COL + D
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NUM_THREADS = 192;
+    static constexpr int PRODUCER_WARP = 4;
+    static constexpr int MMA_WARP = 5;
+    static_assert(D == 64 || D == 128, "backward head dim");
+    static_assert(ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
+    static_assert(NSLOT >= 4, "ring too small");
+};
+
+struct alignas(8) BwdBars {
+    uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
+    uint64_t ring_full[8], ring_empty[8];
+    uint64_t s_full, p_full, acc_done, acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
+{
+    atomicExch(p.status, kStatusTimeout);
+    *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
+}
+
+// Tiles of the other operand that tile t (rows [128 t, 128 t + 128)) meets under the
+// mask: for a query tile, the key tiles [lo, hi); for a key tile (transposed), the
+// query tiles.
+__device__ __forceinline__ void bwd_range(const BwdParams& p, int t, bool key_tile, int& lo, int& hi)
+{
+    const int a = t * 128, last = min(p.N, a + 128) - 1;
+    lo = 0;
+    hi = p.nt;
+    if (!key_tile) {
+        if (p.causal) hi = min(hi, last / 128 + 1);
+        else if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
+        if (p.window > 0) lo = max(0, (a - p.window) / 128);
+    } else {
+        // queries i with some allowed key j in [a, last]: causal i >= j, window |i - j| <= w
+        if (p.causal) lo = a / 128;
+        else if (p.window > 0) lo = max(0, (a - p.window) / 128);
+        if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
+    }
+    if (lo >= hi) hi = lo + 1;  // never empty (cannot happen for the masks above)
+}
+
+// D_i = dO_i . O_i in fp32, one warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const BwdParams p)
+{
+    constexpr int E = D / 32;
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)p.BH * p.N) return;
+    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o) + row * D + lane * E;
+    const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * E;
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) p.delta[row] = acc;
+}
+
+// Common kernel skeleton: setup, the producer, the final drain.  `kDQ` selects the
+// pass: the dQ pass's unit is a query tile (fixed tiles Q, dO; ring K, V), the dK/dV
+// pass's unit is a key tile (fixed tiles K, V; ring Q, dO).
+template <int D, bool kDQ>
+__global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* fix = smem;                                   // 2 tiles
+    uint8_t* ring = smem + 2 * C::TILE_BYTES;              // NSLOT tiles
+    BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::TILE_BYTES);
+    const volatile int* abort_flag = &bars->abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = p.BH * p.nt;
+    // fixed tiles and ring tiles of this pass: dQ pass (Q, dO | K, V); dK/dV pass (K, V | Q, dO)
+    const CUtensorMap* fixA = kDQ ? &tmQ : &tmK;
+    const CUtensorMap* fixB = kDQ ? &tmO : &tmV;   // tmO maps dO
+    const CUtensorMap* ringA = kDQ ? &tmK : &tmQ;
+    const CUtensorMap* ringB = kDQ ? &tmV : &tmO;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->fix_full), 1);
+        mbar_init(smem_u32(&bars->fix_empty), 1);
+        for (int s = 0; s < C::NSLOT; ++s) {
+            mbar_init(smem_u32(&bars->ring_full[s]), 1);
+            mbar_init(smem_u32(&bars->ring_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->p_full), 4);
+        mbar_init(smem_u32(&bars->acc_done), 1);
+        mbar_init(smem_u32(&bars->acc_empty), 4);
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::MMA_WARP) {
+        tmem_alloc(smem_u32(&bars->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == C::PRODUCER_WARP) {
+        if (lane == 0) {
+            const uint64_t pol_fix = l2_policy_evict_first();
+            const uint64_t pol_ring = l2_policy_evict_last();
+            uint32_t rc = 0, uc = 0, armed = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+                const int bh = u / p.nt, t = u - bh * p.nt;
+                int lo, hi;
+                bwd_range(p, t, !kDQ, lo, hi);
+                if (!mbar_wait(smem_u32(&bars->fix_empty), (uc & 1) ^ 1, abort_flag, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bars->fix_full);
+                mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES);
+                ++armed;
+#pragma unroll
+                for (int cb = 0; cb < C::NCB; ++cb) {
+                    tma_load_3d(smem_u32(fix + cb * C::CB_BYTES), fixA, fb, cb * 64, t * 128, bh, pol_fix);
+                    tma_load_3d(smem_u32(fix + C::TILE_BYTES + cb * C::CB_BYTES), fixB, fb, cb * 64,
+                                t * 128, bh, pol_fix);
+                }
+                for (int jj = lo; jj < hi && ok; ++jj) {
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t slot = rc % C::NSLOT;
+                        if (!mbar_wait(smem_u32(&bars->ring_empty[slot]), ((rc / C::NSLOT) & 1) ^ 1,
+                                       abort_flag, p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t rb = smem_u32(&bars->ring_full[slot]);
+                        mbar_arrive_expect_tx(rb, C::TILE_BYTES);
+                        const CUtensorMap* map = which == 0 ? ringA : ringB;
+#pragma unroll
+                        for (int cb = 0; cb < C::NCB; ++cb)
+                            tma_load_3d(smem_u32(ring + slot * C::TILE_BYTES + cb * C::CB_BYTES), map, rb,
+                                        cb * 64, jj * 128, bh, pol_ring);
+                        ++rc;
+                    }
+                }
+            }
+            if (!ok) {
+                bwd_timeout(p, bars);
+                const uint32_t n = rc < C::NSLOT ? rc : C::NSLOT;
+                for (uint32_t k = rc - n; k < rc; ++k)
+                    mbar_wait(smem_u32(&bars->ring_full[k % C::NSLOT]), (k / C::NSLOT) & 1, nullptr,
+                              p.timeout_ns);
+                if (armed > 0)
+                    mbar_wait(smem_u32(&bars->fix_full), (armed - 1) & 1, nullptr, p.timeout_ns);
+            }
+        }
+    } else if (warp == C::MMA_WARP) {
+        constexpr uint32_t idesc_kk = idesc_f32acc(1, 0, 128, 128);  // bf16, both K-major, N = 128
+        constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);   // B MN-major, N = D
+        const uint64_t fixA_k = sdesc_sw128(smem_u32(fix), 16, 1024);
+        const uint64_t fixB_k = sdesc_sw128(smem_u32(fix + C::TILE_BYTES), 16, 1024);
+        const uint64_t ring_k = sdesc_sw128(smem_u32(ring), 16, 1024);
+        const uint64_t ring_mn = sdesc_sw128(smem_u32(ring), C::CB_BYTES, 1024);
+        uint32_t rc = 0, uc = 0, p_phase = 0;
+        bool ok = true;
+        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
+            r = __all_sync(0xffffffffu, r);
+            if (!r) ok = false;
+            return r;
+        };
+        auto commit = [&](uint64_t* bar) { mma_commit_warp(smem_u32(bar)); };
+        // D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major tiles (K = D)
+        auto mm_kk = [&](uint32_t d_col, uint64_t a0, uint64_t b0) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int byte = kk * 32;
+                const uint32_t off = ((byte / 128) * C::CB_BYTES + (byte % 128)) >> 4;
+                mma_ss_warp<false>(tmem + d_col, a0 + off, b0 + off, idesc_kk, kk > 0 ? 1u : 0u);
+            }
+        };
+        // acc[128 x D] (+)= A (TMEM, 128 x 128 bf16 at a_col) * B (ring tile as MN-major, K = 128 rows)
+        auto mm_acc = [&](uint32_t acc_col, uint32_t a_col, uint64_t bmn, bool accumulate) {
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk)
+                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + kk * 8, bmn + ((kk * 16 * 128) >> 4),
+                                   idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
+        };
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+            const int bh = u / p.nt, t = u - bh * p.nt;
+            (void)bh;
+            int lo, hi;
+            bwd_range(p, t, !kDQ, lo, hi);
+            if (!wait(&bars->fix_full, uc & 1)) break;
+            tc_fence_after_sync();
+            for (int jj = lo; jj < hi && ok; ++jj) {
+                const uint32_t sa = rc % C::NSLOT, sb = (rc + 1) % C::NSLOT;
+                if (!wait(&bars->ring_full[sa], (rc / C::NSLOT) & 1)) break;
+                if (!wait(&bars->ring_full[sb], ((rc + 1) / C::NSLOT) & 1)) break;
+                tc_fence_after_sync();
+                const uint64_t ra = ring_k + (uint64_t)((sa * C::TILE_BYTES) >> 4);
+                const uint64_t rbk = ring_k + (uint64_t)((sb * C::TILE_BYTES) >> 4);
+                if constexpr (kDQ) {
+                    mm_kk(C::S_COL, fixA_k, ra);    // S = Q K^T
+                    mm_kk(C::DP_COL, fixB_k, rbk);  // dP = dO V^T
+                } else {
+                    mm_kk(C::S_COL, fixA_k, ra);    // S^T = K Q^T
+                    mm_kk(C::DP_COL, fixB_k, rbk);  // dP^T = V dO^T
+                }
+                commit(&bars->s_full);
+                if (jj == hi - 1) commit(&bars->fix_empty);
+                if (!wait(&bars->p_full, p_phase)) break;
+                p_phase ^= 1;
+                if (jj == lo && !wait(&bars->acc_empty, (uc & 1) ^ 1)) break;
+                tc_fence_after_sync();
+                const uint64_t ma = ring_mn + (uint64_t)((sa * C::TILE_BYTES) >> 4);
+                const uint64_t mb = ring_mn + (uint64_t)((sb * C::TILE_BYTES) >> 4);
+                if constexpr (kDQ) {
+                    mm_acc(C::ACC_COL, C::S_COL, ma, jj > lo);               // dQ += dS K
+                } else {
+                    mm_acc(C::ACC_COL, C::S_COL, mb, jj > lo);               // dV += P^T dO
+                    mm_acc(C::ACC_COL + D, C::DP_COL, ma, jj > lo);          // dK += dS^T Q
+                }
+                commit(&bars->ring_empty[sa]);
+                commit(&bars->ring_empty[sb]);
+                if (jj == hi - 1) commit(&bars->acc_done);
+                rc += 2;
+            }
+        }
+        if (!ok && lane == 0) bwd_timeout(p, bars);
+        commit(&bars->drain);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------------- compute warpgroup
+        const int trow = warp * 32 + lane;              // row of this thread in the tile
+        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const float NEG_INF = -__int_as_float(0x7f800000);
+        const float LOG2E = 1.4426950408889634f;
+        uint32_t s_phase = 0, uc = 0;
+        bool ok = true;
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
+            r = __all_sync(0xffffffffu, r);
+            if (!r) ok = false;
+            return r;
+        };
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+            const int bh = u / p.nt, t = u - bh * p.nt;
+            int lo, hi;
+            bwd_range(p, t, !kDQ, lo, hi);
+            const int my = t * 128 + trow;              // this thread's row (query or key)
+            const bool valid = my < p.N;
+            // dQ pass: per-row LSE and D; dK/dV pass: per-column values come from global below
+            float lse2 = 0.0f, dlt = 0.0f;
+            if constexpr (kDQ) {
+                lse2 = valid ? p.lse[(size_t)bh * p.N + my] * LOG2E : 0.0f;
+                dlt = valid ? p.delta[(size_t)bh * p.N + my] : 0.0f;
+            }
+            for (int jj = lo; jj < hi; ++jj) {
+                if (!wait_all(&bars->s_full, s_phase)) break;
+                s_phase ^= 1;
+                tc_fence_after_sync();
+                const int c0 = jj * 128;                // first column (key / query) of the step
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[64], dr[64];
+                    const uint32_t base = tmem + lane_addr;
+                    tmem_ld32p(base + C::S_COL + half * 64, sr);
+                    tmem_ld32p(base + C::S_COL + half * 64 + 32, sr + 32);
+                    tmem_ld32p(base + C::DP_COL + half * 64, dr);
+                    tmem_ld32p(base + C::DP_COL + half * 64 + 32, dr + 32);
+                    tmem_wait_ld_only();
+                    reg_fence32(sr);
+                    reg_fence32(sr + 32);
+                    reg_fence32(dr);
+                    reg_fence32(dr + 32);
+                    uint32_t pk[32], pkp[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float pv[2], dsv[2];
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int col = c0 + half * 64 + 2 * e + h2;   // the other index
+                            const int qi = kDQ ? my : col, kj = kDQ ? col : my;
+                            bool allow = valid && col < p.N && kj <= qi + (p.causal ? 0 : 0x3fffffff);
+                            if (p.window > 0) allow = allow && kj >= qi - p.window && (p.causal || kj <= qi + p.window);
+                            float l2, dl;
+                            if constexpr (kDQ) {
+                                l2 = lse2;
+                                dl = dlt;
+                            } else {
+                                const size_t ci = (size_t)bh * p.N + min(col, p.N - 1);
+                                l2 = __ldg(p.lse + ci) * LOG2E;
+                                dl = __ldg(p.delta + ci);
+                            }
+                            const float sv = __uint_as_float(sr[2 * e + h2]);
+                            const float pr = allow ? ex2(fmaf(sv, p.c_log2, -l2)) : 0.0f;
+                            pv[h2] = pr;
+                            dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
+                        }
+                        pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                        pkp[e] = pack_bf16x2(pv[0], pv[1]);
+                    }
+                    if constexpr (kDQ) {
+                        tmem_st32p(base + C::S_COL + half * 32, pk);          // dS over S
+                    } else {
+                        tmem_st32p(base + C::S_COL + half * 32, pkp);         // P^T over S^T
+                        tmem_st32p(base + C::DP_COL + half * 32, pk);         // dS^T over dP^T
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+            }
+            if (!ok) break;
+            // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16
+            if (!wait_all(&bars->acc_done, uc & 1)) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int which = 0; which < (kDQ ? 1 : 2); ++which) {
+                const float f = kDQ ? p.scale : (which == 0 ? 1.0f : p.scale);
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(kDQ ? p.dq : (which == 0 ? p.dv : p.dk));
+                out += ((size_t)bh * p.N + my) * D;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_addr + C::ACC_COL + which * D + ch * 32, r);
+                    tmem_wait_ld(r);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * f, __uint_as_float(r[2 * e + 1]) * f);
+                    if (valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+        }
+        if (!ok) bwd_timeout(p, bars);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const BwdParams& p, int sm_count, cudaStream_t stream)
+{
+    using C = BwdCfg<D>;
+    const long long rows = (long long)p.BH * p.N;
+    bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int units = p.BH * p.nt;
+    const int grid = units < sm_count ? units : sm_count;
+    auto kq = bwd_kernel<D, true>;
+    auto kkv = bwd_kernel<D, false>;
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    kq<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kkv<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mdo, const BwdParams& p, int d, int sm_count,
+                       cudaStream_t stream)
+{
+    if (d == 64) return launch_bwd_t<64>(mq, mk, mv, mdo, p, sm_count, stream);
+    if (d == 128) return launch_bwd_t<128>(mq, mk, mv, mdo, p, sm_count, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gb300

@@ -35,6 +35,24 @@ struct FwdParams {
     int T;
 };
 
+// Backward pass (attn_bwd.cu).  Tensors [BH, N, D] bf16; lse / delta [BH, N] fp32.
+struct BwdParams {
+    const void* o;        // forward output
+    const void* dout;     // upstream gradient dO
+    const float* lse;     // forward LSE (natural log)
+    float* delta;         // D_i = dO_i . O_i, written by the pre-pass
+    void* dq;
+    void* dk;
+    void* dv;
+    int* status;          // device status word (timeouts)
+    int BH, N;
+    int nt;               // 128-row tiles per head
+    int causal, window;
+    float c_log2;         // scale * log2(e)
+    float scale;
+    unsigned long long timeout_ns;
+};
+
 // One decoding step over a paged KV cache (decode.cu).
 struct DecodeParams {
     const void* q;        // bf16 [B, H, nq, D]

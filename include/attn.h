@@ -65,6 +65,26 @@ attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o
                             void* stream);
 
 /*
+ * attn_bwd_bf16 -- backward pass of attn_fwd_bf16: dQ, dK, dV for an upstream dO.
+ *
+ * The step after the forward pass ([YT] §1.1; [JJ] §2.3 names the forward pass).
+ * With P = exp(scale * Q K^T + mask - LSE) (the forward's LSE, so P is normalised):
+ *     D_i = dO_i . O_i,  dP = dO V^T,  dS = P * (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO.
+ *   q, k, v, o, dout : const bf16 [B, H, N, d]; o and lse as attn_fwd_bf16 wrote them
+ *   lse        : const float [B, H, N] (natural log)
+ *   dq, dk, dv : bf16 [B, H, N, d], written
+ *   workspace  : device memory of attn_bwd_workspace_bytes(B, H, N) bytes (holds D)
+ *   d in {64, 128}; scale, causal, window as the forward call that made o and lse
+ * Alignment: tensors 16 bytes; lse and workspace 4 bytes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N);
+attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float scale, int causal, int window, void* stream);
+
+/*
  * attn_fwd_bf16_varlen -- attn_fwd_bf16 over variable-length sequences packed
  * without padding.
  *
