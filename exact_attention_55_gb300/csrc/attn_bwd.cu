@@ -36,7 +36,7 @@ struct BwdCfg {
     static constexpr int CB_BYTES = BT * 128;
     static constexpr int TILE_BYTES = NCB * CB_BYTES;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = 1024;
+    static constexpr int BAR_BYTES = 3072;       // barriers + the staged LSE / D columns
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * TILE_BYTES) / TILE_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
@@ -53,14 +53,20 @@ struct BwdCfg {
     static_assert(NSLOT >= 4, "ring too small");
 };
 
-struct alignas(8) BwdBars {
+struct alignas(16) BwdBars {
     uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
     uint64_t ring_full[8], ring_empty[8];
     uint64_t s_full, p_full, acc_done, acc_empty;
+    uint64_t col_ready[2];               // dK/dV pass: the four compute warps staged a column set
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    // dK/dV pass: LSE (log2 units) and D of the step's 128 query columns, double-buffered
+    // by step parity and filled by the compute threads themselves
+    alignas(16) float col_lse2[2][128];
+    alignas(16) float col_delta[2][128];
 };
+static_assert(sizeof(BwdBars) <= 3072, "barrier block");
 
 __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
 {
@@ -143,6 +149,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         mbar_init(smem_u32(&bars->p_full), 4);
         mbar_init(smem_u32(&bars->acc_done), 1);
         mbar_init(smem_u32(&bars->acc_empty), 4);
+        mbar_init(smem_u32(&bars->col_ready[0]), 4);
+        mbar_init(smem_u32(&bars->col_ready[1]), 4);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
         const float NEG_INF = -__int_as_float(0x7f800000);
         const float LOG2E = 1.4426950408889634f;
-        uint32_t s_phase = 0, uc = 0;
+        uint32_t s_phase = 0, uc = 0, colstep = 0;
         bool ok = true;
         auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
@@ -313,10 +321,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 dlt = valid ? p.delta[(size_t)bh * p.N + my] : 0.0f;
             }
             for (int jj = lo; jj < hi; ++jj) {
+                const int c0 = jj * 128;                // first column (key / query) of the step
+                const int cb = colstep & 1;
+                if constexpr (!kDQ) {
+                    // stage this step's column values (one per thread).  Every warp arrives
+                    // only after finishing the step before, the buffer's previous user was
+                    // two steps back, so once col_ready completes the buffer is consistent.
+                    const int col = min(c0 + trow, p.N - 1);
+                    bars->col_lse2[cb][trow] = __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E;
+                    bars->col_delta[cb][trow] = __ldg(p.delta + (size_t)bh * p.N + col);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars->col_ready[cb]));
+                    if (!wait_all(&bars->col_ready[cb], (colstep >> 1) & 1)) break;
+                }
+                ++colstep;
                 if (!wait_all(&bars->s_full, s_phase)) break;
                 s_phase ^= 1;
                 tc_fence_after_sync();
-                const int c0 = jj * 128;                // first column (key / query) of the step
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t sr[64], dr[64];
@@ -345,9 +366,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                                 l2 = lse2;
                                 dl = dlt;
                             } else {
-                                const size_t ci = (size_t)bh * p.N + min(col, p.N - 1);
-                                l2 = __ldg(p.lse + ci) * LOG2E;
-                                dl = __ldg(p.delta + ci);
+                                l2 = bars->col_lse2[cb][half * 64 + 2 * e + h2];
+                                dl = bars->col_delta[cb][half * 64 + 2 * e + h2];
                             }
                             const float sv = __uint_as_float(sr[2 * e + h2]);
                             const float pr = allow ? ex2(fmaf(sv, p.c_log2, -l2)) : 0.0f;
