@@ -10,10 +10,10 @@
 // §2.3 speaks of the forward pass); the formulas are the chain rule through the
 // forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
 //   bwd_dot_kernel   D_i, one warp per row;
-//   bwd_dq_kernel    per 128-row query tile: S = Q K_j^T and dP = dO V_j^T into TMEM,
+//   bwd_kernel<D, true>   (dQ pass) per 128-row query tile: S = Q K_j^T and dP = dO V_j^T into TMEM,
 //                    the compute warpgroup turns them into dS (bf16, over S), then
 //                    dQ += dS K_j; K_j serves as the MN-major operand of the last MMA;
-//   bwd_dkdv_kernel  per 128-key tile, the transposed products: S^T = K Q_i^T and
+//   bwd_kernel<D, false> (dK/dV pass) per 128-key tile, the transposed products: S^T = K Q_i^T and
 //                    dP^T = V dO_i^T, then dV += P^T dO_i and dK += dS^T Q_i.
 // S is recomputed in both passes (7 matmuls per tile pair instead of 5) to keep dQ in
 // TMEM rather than in a global fp32 buffer updated by atomics.
@@ -23,6 +23,8 @@
 // tcgen05.mma.  Every wait is bounded and gives up with ATTN_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "attn_params.h"
 #include "ptx.cuh"
@@ -93,6 +95,22 @@ __device__ __forceinline__ void bwd_range(const BwdParams& p, int t, bool key_ti
         if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
     }
     if (lo >= hi) hi = lo + 1;  // never empty (cannot happen for the masks above)
+}
+
+// True when every (query, key) pair of the 128 x 128 tile pair starting at query q0 and
+// key k0 lies inside the sequence and is allowed by the mask, so the step needs no
+// per-element test: causal needs the last key at or before the first query, a window
+// the first key within w of the last query (and, without causal, the last key within
+// w after the first query).
+__device__ __forceinline__ bool bwd_tile_full(const BwdParams& p, int q0, int k0)
+{
+    if (q0 + 128 > p.N || k0 + 128 > p.N) return false;
+    if (p.causal && k0 + 127 > q0) return false;
+    if (p.window > 0) {
+        if (k0 < q0 + 127 - p.window) return false;
+        if (!p.causal && k0 + 127 > q0 + p.window) return false;
+    }
+    return true;
 }
 
 // D_i = dO_i . O_i in fp32, one warp per row.
@@ -338,52 +356,69 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 if (!wait_all(&bars->s_full, s_phase)) break;
                 s_phase ^= 1;
                 tc_fence_after_sync();
+                // P and dS of this thread's row, 64 columns at a time; the mask is evaluated
+                // only on tiles that cross the diagonal, a window edge or the sequence end
+                auto step = [&](auto masked_tag) {
+                    constexpr bool kMasked = decltype(masked_tag)::value;
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t sr[64], dr[64];
+                        const uint32_t base = tmem + lane_addr;
+                        tmem_ld32p(base + C::S_COL + half * 64, sr);
+                        tmem_ld32p(base + C::S_COL + half * 64 + 32, sr + 32);
+                        tmem_ld32p(base + C::DP_COL + half * 64, dr);
+                        tmem_ld32p(base + C::DP_COL + half * 64 + 32, dr + 32);
+                        tmem_wait_ld_only();
+                        reg_fence32(sr);
+                        reg_fence32(sr + 32);
+                        reg_fence32(dr);
+                        reg_fence32(dr + 32);
+                        uint32_t pk[32], pkp[32];
+                        float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = l4;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sr[64], dr[64];
-                    const uint32_t base = tmem + lane_addr;
-                    tmem_ld32p(base + C::S_COL + half * 64, sr);
-                    tmem_ld32p(base + C::S_COL + half * 64 + 32, sr + 32);
-                    tmem_ld32p(base + C::DP_COL + half * 64, dr);
-                    tmem_ld32p(base + C::DP_COL + half * 64 + 32, dr + 32);
-                    tmem_wait_ld_only();
-                    reg_fence32(sr);
-                    reg_fence32(sr + 32);
-                    reg_fence32(dr);
-                    reg_fence32(dr + 32);
-                    uint32_t pk[32], pkp[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float pv[2], dsv[2];
-#pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int col = c0 + half * 64 + 2 * e + h2;   // the other index
-                            const int qi = kDQ ? my : col, kj = kDQ ? col : my;
-                            bool allow = valid && col < p.N && kj <= qi + (p.causal ? 0 : 0x3fffffff);
-                            if (p.window > 0) allow = allow && kj >= qi - p.window && (p.causal || kj <= qi + p.window);
-                            float l2, dl;
-                            if constexpr (kDQ) {
-                                l2 = lse2;
-                                dl = dlt;
-                            } else {
-                                l2 = bars->col_lse2[cb][half * 64 + 2 * e + h2];
-                                dl = bars->col_delta[cb][half * 64 + 2 * e + h2];
+                        for (int e = 0; e < 32; ++e) {
+                            if constexpr (!kDQ) {
+                                if ((e & 1) == 0) {   // four columns' LSE and D per vector load
+                                    l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][half * 64 + 2 * e]);
+                                    d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][half * 64 + 2 * e]);
+                                }
                             }
-                            const float sv = __uint_as_float(sr[2 * e + h2]);
-                            const float pr = allow ? ex2(fmaf(sv, p.c_log2, -l2)) : 0.0f;
-                            pv[h2] = pr;
-                            dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
+                            float pv[2], dsv[2];
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                float l2 = lse2, dl = dlt;
+                                if constexpr (!kDQ) {
+                                    l2 = (e & 1) ? (h2 ? l4.w : l4.z) : (h2 ? l4.y : l4.x);
+                                    dl = (e & 1) ? (h2 ? d4.w : d4.z) : (h2 ? d4.y : d4.x);
+                                }
+                                const float sv = __uint_as_float(sr[2 * e + h2]);
+                                float pr = ex2(fmaf(sv, p.c_log2, -l2));
+                                if constexpr (kMasked) {
+                                    const int col = c0 + half * 64 + 2 * e + h2;   // the other index
+                                    const int qi = kDQ ? my : col, kj = kDQ ? col : my;
+                                    bool allow = valid && col < p.N && (!p.causal || kj <= qi);
+                                    if (p.window > 0)
+                                        allow = allow && kj >= qi - p.window && (p.causal || kj <= qi + p.window);
+                                    pr = allow ? pr : 0.0f;
+                                }
+                                pv[h2] = pr;
+                                dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
+                            }
+                            pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                            pkp[e] = pack_bf16x2(pv[0], pv[1]);
                         }
-                        pk[e] = pack_bf16x2(dsv[0], dsv[1]);
-                        pkp[e] = pack_bf16x2(pv[0], pv[1]);
+                        if constexpr (kDQ) {
+                            tmem_st32p(base + C::S_COL + half * 32, pk);          // dS over S
+                        } else {
+                            tmem_st32p(base + C::S_COL + half * 32, pkp);         // P^T over S^T
+                            tmem_st32p(base + C::DP_COL + half * 32, pk);         // dS^T over dP^T
+                        }
                     }
-                    if constexpr (kDQ) {
-                        tmem_st32p(base + C::S_COL + half * 32, pk);          // dS over S
-                    } else {
-                        tmem_st32p(base + C::S_COL + half * 32, pkp);         // P^T over S^T
-                        tmem_st32p(base + C::DP_COL + half * 32, pk);         // dS^T over dP^T
-                    }
-                }
+                };
+                if (bwd_tile_full(p, kDQ ? t * 128 : c0, kDQ ? c0 : t * 128))
+                    step(std::false_type{});
+                else
+                    step(std::true_type{});
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
