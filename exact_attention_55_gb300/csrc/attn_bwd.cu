@@ -47,9 +47,10 @@ struct BwdCfg {
     static constexpr int DP_COL = 128;   // dP (then dS^T in the dK/dV pass)
     static constexpr int ACC_COL = 256;  // dQ, or dV then dK at ACC_COL + D
     static constexpr int TMEM_COLS = 512;
-    static constexpr int NUM_THREADS = 192;
-    static constexpr int PRODUCER_WARP = 4;
-    static constexpr int MMA_WARP = 5;
+    static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, 64 columns each
+    static constexpr int NUM_THREADS = 320;
+    static constexpr int PRODUCER_WARP = 8;
+    static constexpr int MMA_WARP = 9;
     static_assert(D == 64 || D == 128, "backward head dim");
     static_assert(ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
     static_assert(NSLOT >= 4, "ring too small");
@@ -59,7 +60,7 @@ struct alignas(16) BwdBars {
     uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
     uint64_t ring_full[8], ring_empty[8];
     uint64_t s_full, p_full, acc_done, acc_empty;
-    uint64_t col_ready[2];               // dK/dV pass: the four compute warps staged a column set
+    uint64_t col_ready[2];               // dK/dV pass: the eight compute warps staged a column set
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -164,11 +165,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             mbar_init(smem_u32(&bars->ring_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), 4);
+        mbar_init(smem_u32(&bars->p_full), C::COMPUTE_WARPS);
         mbar_init(smem_u32(&bars->acc_done), 1);
-        mbar_init(smem_u32(&bars->acc_empty), 4);
-        mbar_init(smem_u32(&bars->col_ready[0]), 4);
-        mbar_init(smem_u32(&bars->col_ready[1]), 4);
+        mbar_init(smem_u32(&bars->acc_empty), C::COMPUTE_WARPS);
+        mbar_init(smem_u32(&bars->col_ready[0]), C::COMPUTE_WARPS);
+        mbar_init(smem_u32(&bars->col_ready[1]), C::COMPUTE_WARPS);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -260,12 +261,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 mma_ss_warp<false>(tmem + d_col, a0 + off, b0 + off, idesc_kk, kk > 0 ? 1u : 0u);
             }
         };
-        // acc[128 x D] (+)= A (TMEM, 128 x 128 bf16 at a_col) * B (ring tile as MN-major, K = 128 rows)
+        // acc[128 x D] (+)= A (TMEM, 128 x 128 bf16) * B (ring tile as MN-major, K = 128 rows).
+        // A's bf16 pairs for K rows 0-63 sit at a_col + [0, 32), for rows 64-127 at
+        // a_col + [64, 96): each compute warpgroup packs over its own half of the columns.
         auto mm_acc = [&](uint32_t acc_col, uint32_t a_col, uint64_t bmn, bool accumulate) {
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk)
-                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + kk * 8, bmn + ((kk * 16 * 128) >> 4),
-                                   idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
+                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
+                                   bmn + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
             const int bh = u / p.nt, t = u - bh * p.nt;
@@ -312,10 +315,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         commit(&bars->drain);
         mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
         __syncwarp();
-    } else if (warp < 4) {
-        // ---------------------------------------------------------------- compute warpgroup
-        const int trow = warp * 32 + lane;              // row of this thread in the tile
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    } else if (warp < C::COMPUTE_WARPS) {
+        // ---------------------------------------------------------------- compute warpgroups
+        // warpgroup wg owns columns [64 wg, 64 wg + 64) of every step; a warp reaches the
+        // TMEM lanes of its index within the warpgroup
+        const int wg = warp >> 2;
+        const int trow = (warp & 3) * 32 + lane;        // row of this thread in the tile
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const float NEG_INF = -__int_as_float(0x7f800000);
         const float LOG2E = 1.4426950408889634f;
         uint32_t s_phase = 0, uc = 0, colstep = 0;
@@ -345,9 +351,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                     // stage this step's column values (one per thread).  Every warp arrives
                     // only after finishing the step before, the buffer's previous user was
                     // two steps back, so once col_ready completes the buffer is consistent.
+                    // warpgroup 0 loads the LSE, warpgroup 1 the D of the 128 columns
                     const int col = min(c0 + trow, p.N - 1);
-                    bars->col_lse2[cb][trow] = __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E;
-                    bars->col_delta[cb][trow] = __ldg(p.delta + (size_t)bh * p.N + col);
+                    if (wg == 0)
+                        bars->col_lse2[cb][trow] = __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E;
+                    else
+                        bars->col_delta[cb][trow] = __ldg(p.delta + (size_t)bh * p.N + col);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&bars->col_ready[cb]));
                     if (!wait_all(&bars->col_ready[cb], (colstep >> 1) & 1)) break;
@@ -356,31 +365,47 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 if (!wait_all(&bars->s_full, s_phase)) break;
                 s_phase ^= 1;
                 tc_fence_after_sync();
-                // P and dS of this thread's row, 64 columns at a time; the mask is evaluated
-                // only on tiles that cross the diagonal, a window edge or the sequence end
+                // P and dS of this thread's row over the warpgroup's 64 columns, 32 at a time;
+                // the mask is evaluated only on tiles that cross the diagonal, a window edge
+                // or the sequence end
                 auto step = [&](auto masked_tag) {
                     constexpr bool kMasked = decltype(masked_tag)::value;
-#pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t sr[64], dr[64];
-                        const uint32_t base = tmem + lane_addr;
-                        tmem_ld32p(base + C::S_COL + half * 64, sr);
-                        tmem_ld32p(base + C::S_COL + half * 64 + 32, sr + 32);
-                        tmem_ld32p(base + C::DP_COL + half * 64, dr);
-                        tmem_ld32p(base + C::DP_COL + half * 64 + 32, dr + 32);
+                    // The columns (the other index) the mask allows for this thread's row form
+                    // one interval [m_lo, m_hi]: for a query row, keys from max(0, i - w) (w > 0)
+                    // to i (causal) or i + w (window) or N - 1; for a key row, queries from j
+                    // (causal) or j - w (window) or 0, to j + w (window) or N - 1.  One unsigned
+                    // compare per element tests it.  A row past N gets some interval: its
+                    // values stay finite and are never stored (row r of a product depends on
+                    // row r of the TMEM operand only).
+                    int m_lo, m_hi;
+                    if constexpr (kDQ) {
+                        m_lo = p.window > 0 ? my - p.window : 0;
+                        m_hi = p.causal ? my : (p.window > 0 ? my + p.window : p.N - 1);
+                    } else {
+                        m_lo = p.causal ? my : (p.window > 0 ? my - p.window : 0);
+                        m_hi = p.window > 0 ? my + p.window : p.N - 1;
+                    }
+                    m_hi = min(m_hi, p.N - 1);
+                    const uint32_t m_span = (uint32_t)(m_hi - m_lo);
+                    const uint32_t base = tmem + lane_addr;
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const int cc = wg * 64 + ch * 32;       // first column of the chunk
+                        uint32_t sr[32], dr[32];
+                        tmem_ld32p(base + C::S_COL + cc, sr);
+                        tmem_ld32p(base + C::DP_COL + cc, dr);
                         tmem_wait_ld_only();
                         reg_fence32(sr);
-                        reg_fence32(sr + 32);
                         reg_fence32(dr);
-                        reg_fence32(dr + 32);
-                        uint32_t pk[32], pkp[32];
-                        float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = l4;
+                        uint32_t pk[16];
+                        [[maybe_unused]] uint32_t pkp[16];
+                        [[maybe_unused]] float4 l4, d4;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
+                        for (int e = 0; e < 16; ++e) {
                             if constexpr (!kDQ) {
                                 if ((e & 1) == 0) {   // four columns' LSE and D per vector load
-                                    l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][half * 64 + 2 * e]);
-                                    d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][half * 64 + 2 * e]);
+                                    l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][cc + 2 * e]);
+                                    d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][cc + 2 * e]);
                                 }
                             }
                             float pv[2], dsv[2];
@@ -394,24 +419,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                                 const float sv = __uint_as_float(sr[2 * e + h2]);
                                 float pr = ex2(fmaf(sv, p.c_log2, -l2));
                                 if constexpr (kMasked) {
-                                    const int col = c0 + half * 64 + 2 * e + h2;   // the other index
-                                    const int qi = kDQ ? my : col, kj = kDQ ? col : my;
-                                    bool allow = valid && col < p.N && (!p.causal || kj <= qi);
-                                    if (p.window > 0)
-                                        allow = allow && kj >= qi - p.window && (p.causal || kj <= qi + p.window);
-                                    pr = allow ? pr : 0.0f;
+                                    // column c0 + cc + 2e + h2 is allowed iff it lies in [lo, hi]
+                                    const uint32_t off = (uint32_t)(c0 + cc - m_lo) + (uint32_t)(2 * e + h2);
+                                    pr = off <= m_span ? pr : 0.0f;
                                 }
                                 pv[h2] = pr;
                                 dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
                             }
                             pk[e] = pack_bf16x2(dsv[0], dsv[1]);
-                            pkp[e] = pack_bf16x2(pv[0], pv[1]);
+                            if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
                         }
+                        // bf16 pairs: the chunk's 32 columns fill 16 packed TMEM columns at
+                        // 64 wg + 16 ch, inside this warpgroup's own S (dP) columns whose values
+                        // it has already loaded; the other warpgroup's columns are untouched
+                        const uint32_t pc = (uint32_t)(wg * 64 + ch * 16);
                         if constexpr (kDQ) {
-                            tmem_st32p(base + C::S_COL + half * 32, pk);          // dS over S
+                            tmem_st16p(base + C::S_COL + pc, pk);             // dS over S
                         } else {
-                            tmem_st32p(base + C::S_COL + half * 32, pkp);         // P^T over S^T
-                            tmem_st32p(base + C::DP_COL + half * 32, pk);         // dS^T over dP^T
+                            tmem_st16p(base + C::S_COL + pc, pkp);            // P^T over S^T
+                            tmem_st16p(base + C::DP_COL + pc, pk);            // dS^T over dP^T
                         }
                     }
                 };
@@ -428,13 +454,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16
             if (!wait_all(&bars->acc_done, uc & 1)) break;
             tc_fence_after_sync();
-#pragma unroll
-            for (int which = 0; which < (kDQ ? 1 : 2); ++which) {
+            // dQ pass: each warpgroup writes half of dQ's columns; dK/dV pass: warpgroup 0
+            // writes dV, warpgroup 1 dK
+            {
+                const int which = kDQ ? 0 : wg;
                 const float f = kDQ ? p.scale : (which == 0 ? 1.0f : p.scale);
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(kDQ ? p.dq : (which == 0 ? p.dv : p.dk));
                 out += ((size_t)bh * p.N + my) * D;
+                constexpr int NCH = kDQ ? D / 64 : D / 32;     // 32-column chunks per warpgroup
+                const int ch0 = kDQ ? wg * NCH : 0;
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
+                for (int ci = 0; ci < NCH; ++ci) {
+                    const int ch = ch0 + ci;
                     uint32_t r[32];
                     tmem_ld32(tmem + lane_addr + C::ACC_COL + which * D + ch * 32, r);
                     tmem_wait_ld(r);

@@ -301,6 +301,16 @@ __device__ __forceinline__ void tmem_st32p(uint32_t taddr, const uint32_t* r)
         : "memory");
 }
 
+// 16 registers r[0..15] of a longer array to 16 consecutive TMEM columns.
+__device__ __forceinline__ void tmem_st16p(uint32_t taddr, const uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        GB300_W8(0), GB300_W8(8)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
 {
     asm volatile(
