@@ -479,6 +479,29 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     gbs = dbytes / (statistics.mean(per) * 1e-3) / 1e9
     out["decode_paged_noalloc"] = {"GB_per_s": gbs, "frac_of_hbm": gbs / hbm,
                                    "us": 1e3 * statistics.mean(per)}
+    del dq_, dkc, dvc, dpt, dsl, do_, dl_, dws
+    # backward pass on the headline shape: dO seeded on the device; FLOPs counted as
+    # 2.5 x the forward's (five N x N x d products), halved under the causal mask; the
+    # kernels run seven such products (S is recomputed in both passes)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    dout = torch.randn(qd.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dqb, dkb, dvb = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    bws = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        fa.attn_fwd_bf16(qd, kd, vd, scale=scale, causal=causal, o=o, lse=lse, stream=stream)
+
+        def bwd_step():
+            fa.attn_bwd_bf16(qd, kd, vd, o, dout, lse, scale=scale, causal=causal, dq=dqb, dk=dkb,
+                             dv=dvb, workspace=bws, stream=stream)
+        ms, per = time_steps(bwd_step, reps, 3, stream)
+        f = 2.5 * flops(B, H, N, D, causal=causal)
+        t = f / (statistics.mean(per) * 1e-3) / 1e12
+        out["bwd_causal" if causal else "bwd"] = {
+            "tflops": t, "ms": statistics.mean(per), "flop_count": "2.5 x forward (10 N^2 d per head)",
+            "tensor_tflops_executed": t * 7.0 / 5.0,
+            "frac_of_peak": t / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))}
+    del dout, dqb, dkb, dvb, bws
     status = fa.attn_get_device_status()
     out["device_status"] = status
     return out
@@ -508,6 +531,14 @@ def run_profile_case(args):
     elif args.profile == "quant_hadamard":
         def run():
             fa.attn_quantize_fp8_hadamard(qd)
+    elif args.profile == "bwd":
+        o, lse = fa.attn_fwd_bf16(qd, kd, vd, scale=scale)
+        gen = torch.Generator(device=qd.device)
+        gen.manual_seed(11)
+        dout = torch.randn(qd.shape, generator=gen, device=qd.device).to(torch.bfloat16)
+
+        def run():
+            fa.attn_bwd_bf16(qd, kd, vd, o, dout, lse, scale=scale)
     elif args.profile == "decode":
         from exact_attention_55_gb300.inputs import make_paged_cache
         dq_, dkc, dvc, dpt, dsl = (t.cuda() for t in make_paged_cache([n] * 8, h, 1, d, 64, seed=0))
@@ -591,7 +622,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
     ap.add_argument("--profile", default=None,
                     choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant",
-                             "quant_hadamard", "decode"],
+                             "quant_hadamard", "decode", "bwd"],
                     help="run a small case of one kernel (for ncu) and exit")
     ap.add_argument("--sweep", action="store_true",
                     help="time the d x N x mask sweep (one JSON line per point) and exit")

@@ -21,9 +21,7 @@ namespace gb300 {
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
-cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const BwdParams& p, int d, int sm_count,
-                       cudaStream_t stream);
+cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count, cudaStream_t stream);
 
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
@@ -522,10 +520,15 @@ extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void*
     st = device_info(&dev);
     if (st != ATTN_OK) return st;
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    alignas(64) CUtensorMap mq, mk, mv, mdo;
-    if (!encode_3d(&mq, q, dt, 2, d, N, (int)BH, 128) || !encode_3d(&mk, k, dt, 2, d, N, (int)BH, 128) ||
-        !encode_3d(&mv, v, dt, 2, d, N, (int)BH, 128) || !encode_3d(&mdo, dout, dt, 2, d, N, (int)BH, 128))
-        return ATTN_ERR_CUDA;
+    // 128-row boxes for a unit's fixed tiles, 64-row boxes for the ring tiles of a step
+    alignas(64) BwdMaps maps;
+    const void* src[4] = {q, k, v, dout};
+    CUtensorMap* big[4] = {&maps.q, &maps.k, &maps.v, &maps.dout};
+    CUtensorMap* small[4] = {&maps.q64, &maps.k64, &maps.v64, &maps.dout64};
+    for (int i = 0; i < 4; ++i)
+        if (!encode_3d(big[i], src[i], dt, 2, d, N, (int)BH, 128) ||
+            !encode_3d(small[i], src[i], dt, 2, d, N, (int)BH, 64))
+            return ATTN_ERR_CUDA;
     BwdParams p;
     std::memset(&p, 0, sizeof(p));
     p.o = o;
@@ -544,7 +547,7 @@ extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void*
     p.c_log2 = (float)((double)scale * 1.4426950408889634);
     p.scale = scale;
     p.timeout_ns = kWaitTimeoutNs;
-    if (launch_bwd(mq, mk, mv, mdo, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (launch_bwd(maps, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

@@ -9,18 +9,25 @@
 // V3：优化框架吞吐量的关键技术实践" §1.1; "大模型加速-核心网络算子-Flash Attention V3"
 // §2.3 speaks of the forward pass); the formulas are the chain rule through the
 // forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
-//   bwd_dot_kernel   D_i, one warp per row;
-//   bwd_kernel<D, true>   (dQ pass) per 128-row query tile: S = Q K_j^T and dP = dO V_j^T into TMEM,
-//                    the compute warpgroup turns them into dS (bf16, over S), then
-//                    dQ += dS K_j; K_j serves as the MN-major operand of the last MMA;
-//   bwd_kernel<D, false> (dK/dV pass) per 128-key tile, the transposed products: S^T = K Q_i^T and
-//                    dP^T = V dO_i^T, then dV += P^T dO_i and dK += dS^T Q_i.
+//   bwd_dot_kernel          D_i, one warp per row;
+//   bwd_kernel<D, true>     (dQ pass) per 128-row query tile, in steps of 64 keys:
+//                           S = Q K_j^T and dP = dO V_j^T into TMEM, the compute
+//                           warpgroups turn them into dS (bf16, over S), then
+//                           dQ += dS K_j with K_j as the MN-major operand;
+//   bwd_kernel<D, false>    (dK/dV pass) per 128-key tile, in steps of 64 queries, the
+//                           transposed products: S^T = K Q_i^T and dP^T = V dO_i^T,
+//                           then dV += P^T dO_i and dK += dS^T Q_i.
 // S is recomputed in both passes (7 matmuls per tile pair instead of 5) to keep dQ in
 // TMEM rather than in a global fp32 buffer updated by atomics.
 //
-// Roles per CTA (persistent over units): warps 0-3 compute (one thread per row of the
-// tile), warp 4 streams tiles with TMA through an mbarrier ring, warp 5 issues the
-// tcgen05.mma.  Every wait is bounded and gives up with ATTN_ERR_TIMEOUT.
+// Software pipeline: S and dP of a step live in one of two TMEM buffers, so the MMA
+// warp issues step h's S and dP before step h-1's accumulation and the tensor pipe
+// computes them while the compute warpgroups turn step h-1 into P and dS.
+//
+// Roles per CTA (persistent over units): warps 0-7 compute (two warpgroups, one thread
+// per tile row, each warpgroup 32 of the step's 64 columns), warp 8 streams tiles with
+// TMA through an mbarrier ring, warp 9 issues the tcgen05.mma.  Every wait is bounded
+// and gives up with ATTN_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,43 +40,49 @@ namespace gb300 {
 
 template <int D>
 struct BwdCfg {
-    static constexpr int BT = 128;                 // rows of a query or key tile
+    static constexpr int BT = 128;                 // rows of a unit's tile (query or key)
+    static constexpr int BC = 64;                  // columns of a step (the other index)
     static constexpr int NCB = D / 64;             // 128-byte column blocks of a bf16 row
-    static constexpr int CB_BYTES = BT * 128;
-    static constexpr int TILE_BYTES = NCB * CB_BYTES;
+    static constexpr int FIX_CB = BT * 128;        // one column block of a fixed tile
+    static constexpr int FIX_BYTES = NCB * FIX_CB;
+    static constexpr int RING_CB = BC * 128;       // one column block of a ring tile
+    static constexpr int RING_BYTES = NCB * RING_CB;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = 3072;       // barriers + the staged LSE / D columns
+    static constexpr int BAR_BYTES = 2048;         // barriers + the staged LSE / D columns
     static constexpr int ALIGN_SLACK = 1024;
-    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * TILE_BYTES) / TILE_BYTES;
+    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * FIX_BYTES) / RING_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
-    static constexpr int SMEM_BYTES = ALIGN_SLACK + (2 + NSLOT) * TILE_BYTES + BAR_BYTES;
-    static constexpr int S_COL = 0;      // S (then dS or P) of the step
-    static constexpr int DP_COL = 128;   // dP (then dS^T in the dK/dV pass)
-    static constexpr int ACC_COL = 256;  // dQ, or dV then dK at ACC_COL + D
+    static constexpr int SMEM_BYTES = ALIGN_SLACK + 2 * FIX_BYTES + NSLOT * RING_BYTES + BAR_BYTES;
+    static constexpr int BUF_COLS = 128;           // TMEM columns of a step buffer
+    static constexpr int S_OFF = 0;                // S (then dS, or P^T) of the step
+    static constexpr int DP_OFF = 64;              // dP (then dS^T in the dK/dV pass)
+    static constexpr int ACC_COL = 256;            // dQ, or dV then dK at ACC_COL + D
     static constexpr int TMEM_COLS = 512;
-    static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, 64 columns each
+    static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, 32 columns each
     static constexpr int NUM_THREADS = 320;
     static constexpr int PRODUCER_WARP = 8;
     static constexpr int MMA_WARP = 9;
     static_assert(D == 64 || D == 128, "backward head dim");
-    static_assert(ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
-    static_assert(NSLOT >= 4, "ring too small");
+    static_assert(2 * BUF_COLS <= ACC_COL && ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
+    static_assert(NSLOT >= 6, "ring too small");
+    static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
 };
 
 struct alignas(16) BwdBars {
     uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
     uint64_t ring_full[8], ring_empty[8];
-    uint64_t s_full, p_full, acc_done, acc_empty;
+    uint64_t s_full[2], p_full[2];       // per TMEM step buffer
+    uint64_t acc_done, acc_empty;
     uint64_t col_ready[2];               // dK/dV pass: the eight compute warps staged a column set
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    // dK/dV pass: LSE (log2 units) and D of the step's 128 query columns, double-buffered
+    // dK/dV pass: LSE (log2 units) and D of a step's 64 query columns, double-buffered
     // by step parity and filled by the compute threads themselves
-    alignas(16) float col_lse2[2][128];
-    alignas(16) float col_delta[2][128];
+    alignas(16) float col_lse2[2][64];
+    alignas(16) float col_delta[2][64];
 };
-static_assert(sizeof(BwdBars) <= 3072, "barrier block");
+static_assert(sizeof(BwdBars) <= 2048, "barrier block");
 
 __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
 {
@@ -77,10 +90,11 @@ __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
 }
 
-// Tiles of the other operand that tile t (rows [128 t, 128 t + 128)) meets under the
-// mask: for a query tile, the key tiles [lo, hi); for a key tile (transposed), the
-// query tiles.
-__device__ __forceinline__ void bwd_range(const BwdParams& p, int t, bool key_tile, int& lo, int& hi)
+// Steps (64-column blocks of the other operand) that tile t (rows [128 t, 128 t + 128))
+// meets under the mask: for a query tile, the key blocks [lo, hi); for a key tile
+// (transposed), the query blocks.  Computed on 128-column tiles, then split in two and
+// cut at the sequence end.
+__device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_tile, int& lo, int& hi)
 {
     const int a = t * 128, last = min(p.N, a + 128) - 1;
     lo = 0;
@@ -96,20 +110,22 @@ __device__ __forceinline__ void bwd_range(const BwdParams& p, int t, bool key_ti
         if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
     }
     if (lo >= hi) hi = lo + 1;  // never empty (cannot happen for the masks above)
+    lo *= 2;
+    hi = min(2 * hi, (p.N + 63) / 64);
 }
 
-// True when every (query, key) pair of the 128 x 128 tile pair starting at query q0 and
-// key k0 lies inside the sequence and is allowed by the mask, so the step needs no
-// per-element test: causal needs the last key at or before the first query, a window
+// True when every (query, key) pair of the block of queries [q0, q0 + nq) and keys
+// [k0, k0 + nk) lies inside the sequence and is allowed by the mask, so the step needs
+// no per-element test: causal needs the last key at or before the first query, a window
 // the first key within w of the last query (and, without causal, the last key within
 // w after the first query).
-__device__ __forceinline__ bool bwd_tile_full(const BwdParams& p, int q0, int k0)
+__device__ __forceinline__ bool bwd_block_full(const BwdParams& p, int q0, int nq, int k0, int nk)
 {
-    if (q0 + 128 > p.N || k0 + 128 > p.N) return false;
-    if (p.causal && k0 + 127 > q0) return false;
+    if (q0 + nq > p.N || k0 + nk > p.N) return false;
+    if (p.causal && k0 + nk - 1 > q0) return false;
     if (p.window > 0) {
-        if (k0 < q0 + 127 - p.window) return false;
-        if (!p.causal && k0 + 127 > q0 + p.window) return false;
+        if (k0 < q0 + nq - 1 - p.window) return false;
+        if (!p.causal && k0 + nk - 1 > q0 + p.window) return false;
     }
     return true;
 }
@@ -132,30 +148,25 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const BwdParams p)
     if (lane == 0) p.delta[row] = acc;
 }
 
-// Common kernel skeleton: setup, the producer, the final drain.  `kDQ` selects the
-// pass: the dQ pass's unit is a query tile (fixed tiles Q, dO; ring K, V), the dK/dV
-// pass's unit is a key tile (fixed tiles K, V; ring Q, dO).
+// One pass.  `kDQ` selects it: the dQ pass's unit is a query tile (fixed tiles Q, dO;
+// ring K, V), the dK/dV pass's unit is a key tile (fixed tiles K, V; ring Q, dO).  The
+// fixed maps have 128-row boxes, the ring maps 64-row boxes.
 template <int D, bool kDQ>
 __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
-    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+    bwd_kernel(const __grid_constant__ CUtensorMap tmFixA, const __grid_constant__ CUtensorMap tmFixB,
+               const __grid_constant__ CUtensorMap tmRingA, const __grid_constant__ CUtensorMap tmRingB,
                const BwdParams p)
 {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* fix = smem;                                   // 2 tiles
-    uint8_t* ring = smem + 2 * C::TILE_BYTES;              // NSLOT tiles
-    BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::TILE_BYTES);
+    uint8_t* fix = smem;                                   // 2 fixed tiles
+    uint8_t* ring = smem + 2 * C::FIX_BYTES;               // NSLOT ring tiles
+    BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::RING_BYTES);
     const volatile int* abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = p.BH * p.nt;
-    // fixed tiles and ring tiles of this pass: dQ pass (Q, dO | K, V); dK/dV pass (K, V | Q, dO)
-    const CUtensorMap* fixA = kDQ ? &tmQ : &tmK;
-    const CUtensorMap* fixB = kDQ ? &tmO : &tmV;   // tmO maps dO
-    const CUtensorMap* ringA = kDQ ? &tmK : &tmQ;
-    const CUtensorMap* ringB = kDQ ? &tmV : &tmO;
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->fix_full), 1);
@@ -164,12 +175,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             mbar_init(smem_u32(&bars->ring_full[s]), 1);
             mbar_init(smem_u32(&bars->ring_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), C::COMPUTE_WARPS);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->s_full[b]), 1);
+            mbar_init(smem_u32(&bars->p_full[b]), C::COMPUTE_WARPS);
+            mbar_init(smem_u32(&bars->col_ready[b]), C::COMPUTE_WARPS);
+        }
         mbar_init(smem_u32(&bars->acc_done), 1);
         mbar_init(smem_u32(&bars->acc_empty), C::COMPUTE_WARPS);
-        mbar_init(smem_u32(&bars->col_ready[0]), C::COMPUTE_WARPS);
-        mbar_init(smem_u32(&bars->col_ready[1]), C::COMPUTE_WARPS);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -192,21 +204,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
                 const int bh = u / p.nt, t = u - bh * p.nt;
                 int lo, hi;
-                bwd_range(p, t, !kDQ, lo, hi);
+                bwd_steps(p, t, !kDQ, lo, hi);
                 if (!mbar_wait(smem_u32(&bars->fix_empty), (uc & 1) ^ 1, abort_flag, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&bars->fix_full);
-                mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES);
+                mbar_arrive_expect_tx(fb, 2 * C::FIX_BYTES);
                 ++armed;
 #pragma unroll
                 for (int cb = 0; cb < C::NCB; ++cb) {
-                    tma_load_3d(smem_u32(fix + cb * C::CB_BYTES), fixA, fb, cb * 64, t * 128, bh, pol_fix);
-                    tma_load_3d(smem_u32(fix + C::TILE_BYTES + cb * C::CB_BYTES), fixB, fb, cb * 64,
+                    tma_load_3d(smem_u32(fix + cb * C::FIX_CB), &tmFixA, fb, cb * 64, t * 128, bh, pol_fix);
+                    tma_load_3d(smem_u32(fix + C::FIX_BYTES + cb * C::FIX_CB), &tmFixB, fb, cb * 64,
                                 t * 128, bh, pol_fix);
                 }
-                for (int jj = lo; jj < hi && ok; ++jj) {
+                for (int s = lo; s < hi && ok; ++s) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = rc % C::NSLOT;
@@ -216,12 +228,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                             break;
                         }
                         const uint32_t rb = smem_u32(&bars->ring_full[slot]);
-                        mbar_arrive_expect_tx(rb, C::TILE_BYTES);
-                        const CUtensorMap* map = which == 0 ? ringA : ringB;
+                        mbar_arrive_expect_tx(rb, C::RING_BYTES);
+                        const CUtensorMap* map = which == 0 ? &tmRingA : &tmRingB;
 #pragma unroll
                         for (int cb = 0; cb < C::NCB; ++cb)
-                            tma_load_3d(smem_u32(ring + slot * C::TILE_BYTES + cb * C::CB_BYTES), map, rb,
-                                        cb * 64, jj * 128, bh, pol_ring);
+                            tma_load_3d(smem_u32(ring + slot * C::RING_BYTES + cb * C::RING_CB), map, rb,
+                                        cb * 64, s * C::BC, bh, pol_ring);
                         ++rc;
                     }
                 }
@@ -237,13 +249,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             }
         }
     } else if (warp == C::MMA_WARP) {
-        constexpr uint32_t idesc_kk = idesc_f32acc(1, 0, 128, 128);  // bf16, both K-major, N = 128
-        constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);   // B MN-major, N = D
+        constexpr uint32_t idesc_kk = idesc_f32acc(1, 0, 128, C::BC);  // bf16, both K-major, N = 64
+        constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);     // B MN-major, N = D
         const uint64_t fixA_k = sdesc_sw128(smem_u32(fix), 16, 1024);
-        const uint64_t fixB_k = sdesc_sw128(smem_u32(fix + C::TILE_BYTES), 16, 1024);
+        const uint64_t fixB_k = sdesc_sw128(smem_u32(fix + C::FIX_BYTES), 16, 1024);
         const uint64_t ring_k = sdesc_sw128(smem_u32(ring), 16, 1024);
-        const uint64_t ring_mn = sdesc_sw128(smem_u32(ring), C::CB_BYTES, 1024);
-        uint32_t rc = 0, uc = 0, p_phase = 0;
+        const uint64_t ring_mn = sdesc_sw128(smem_u32(ring), C::RING_CB, 1024);
+        uint32_t rc = 0, uc = 0, hs = 0;
         bool ok = true;
         auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
@@ -252,64 +264,74 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             return r;
         };
         auto commit = [&](uint64_t* bar) { mma_commit_warp(smem_u32(bar)); };
-        // D[128 x 128] = A[128 x D] B[128 x D]^T, both K-major tiles (K = D)
+        // D[128 x 64] = A[128 x D] (fixed tile) B[64 x D]^T (ring tile), both K-major, K = D
         auto mm_kk = [&](uint32_t d_col, uint64_t a0, uint64_t b0) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int byte = kk * 32;
-                const uint32_t off = ((byte / 128) * C::CB_BYTES + (byte % 128)) >> 4;
-                mma_ss_warp<false>(tmem + d_col, a0 + off, b0 + off, idesc_kk, kk > 0 ? 1u : 0u);
+                const uint32_t offa = ((byte / 128) * C::FIX_CB + (byte % 128)) >> 4;
+                const uint32_t offb = ((byte / 128) * C::RING_CB + (byte % 128)) >> 4;
+                mma_ss_warp<false>(tmem + d_col, a0 + offa, b0 + offb, idesc_kk, kk > 0 ? 1u : 0u);
             }
         };
-        // acc[128 x D] (+)= A (TMEM, 128 x 128 bf16) * B (ring tile as MN-major, K = 128 rows).
-        // A's bf16 pairs for K rows 0-63 sit at a_col + [0, 32), for rows 64-127 at
-        // a_col + [64, 96): each compute warpgroup packs over its own half of the columns.
+        // acc[128 x D] (+)= A (TMEM, 128 x 64 bf16) * B (ring tile as MN-major, K = 64 rows).
+        // A's bf16 pairs for K rows 0-31 sit at a_col + [0, 16), rows 32-63 at
+        // a_col + [32, 48): each compute warpgroup packs over its own 32 columns.
         auto mm_acc = [&](uint32_t acc_col, uint32_t a_col, uint64_t bmn, bool accumulate) {
 #pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk)
-                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
+            for (int kk = 0; kk < C::BC / 16; ++kk)
+                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + (kk / 2) * 32 + (kk % 2) * 8,
                                    bmn + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-            const int bh = u / p.nt, t = u - bh * p.nt;
-            (void)bh;
             int lo, hi;
-            bwd_range(p, t, !kDQ, lo, hi);
+            bwd_steps(p, u % p.nt, !kDQ, lo, hi);
             if (!wait(&bars->fix_full, uc & 1)) break;
             tc_fence_after_sync();
-            for (int jj = lo; jj < hi && ok; ++jj) {
+            bool acc_started = false;
+            // accumulation of step h (its P / dS are in TMEM once p_full fires), then the
+            // step's two ring tiles are free
+            auto issue_acc = [&](uint32_t h, uint32_t sa, uint32_t sb) -> bool {
+                if (!wait(&bars->p_full[h & 1], (h >> 1) & 1)) return false;
+                if (!acc_started && !wait(&bars->acc_empty, (uc & 1) ^ 1)) return false;
+                tc_fence_after_sync();
+                const uint64_t ma = ring_mn + (uint64_t)((sa * C::RING_BYTES) >> 4);
+                const uint64_t mb = ring_mn + (uint64_t)((sb * C::RING_BYTES) >> 4);
+                const uint32_t bc = (h & 1) * C::BUF_COLS;
+                if constexpr (kDQ) {
+                    mm_acc(C::ACC_COL, bc + C::S_OFF, ma, acc_started);          // dQ += dS K
+                } else {
+                    mm_acc(C::ACC_COL, bc + C::S_OFF, mb, acc_started);          // dV += P^T dO
+                    mm_acc(C::ACC_COL + D, bc + C::DP_OFF, ma, acc_started);     // dK += dS^T Q
+                }
+                acc_started = true;
+                commit(&bars->ring_empty[sa]);
+                commit(&bars->ring_empty[sb]);
+                return true;
+            };
+            uint32_t psa = 0, psb = 0;
+            bool pend = false;
+            for (int s = lo; s < hi; ++s) {
                 const uint32_t sa = rc % C::NSLOT, sb = (rc + 1) % C::NSLOT;
                 if (!wait(&bars->ring_full[sa], (rc / C::NSLOT) & 1)) break;
                 if (!wait(&bars->ring_full[sb], ((rc + 1) / C::NSLOT) & 1)) break;
                 tc_fence_after_sync();
-                const uint64_t ra = ring_k + (uint64_t)((sa * C::TILE_BYTES) >> 4);
-                const uint64_t rbk = ring_k + (uint64_t)((sb * C::TILE_BYTES) >> 4);
-                if constexpr (kDQ) {
-                    mm_kk(C::S_COL, fixA_k, ra);    // S = Q K^T
-                    mm_kk(C::DP_COL, fixB_k, rbk);  // dP = dO V^T
-                } else {
-                    mm_kk(C::S_COL, fixA_k, ra);    // S^T = K Q^T
-                    mm_kk(C::DP_COL, fixB_k, rbk);  // dP^T = V dO^T
-                }
-                commit(&bars->s_full);
-                if (jj == hi - 1) commit(&bars->fix_empty);
-                if (!wait(&bars->p_full, p_phase)) break;
-                p_phase ^= 1;
-                if (jj == lo && !wait(&bars->acc_empty, (uc & 1) ^ 1)) break;
-                tc_fence_after_sync();
-                const uint64_t ma = ring_mn + (uint64_t)((sa * C::TILE_BYTES) >> 4);
-                const uint64_t mb = ring_mn + (uint64_t)((sb * C::TILE_BYTES) >> 4);
-                if constexpr (kDQ) {
-                    mm_acc(C::ACC_COL, C::S_COL, ma, jj > lo);               // dQ += dS K
-                } else {
-                    mm_acc(C::ACC_COL, C::S_COL, mb, jj > lo);               // dV += P^T dO
-                    mm_acc(C::ACC_COL + D, C::DP_COL, ma, jj > lo);          // dK += dS^T Q
-                }
-                commit(&bars->ring_empty[sa]);
-                commit(&bars->ring_empty[sb]);
-                if (jj == hi - 1) commit(&bars->acc_done);
+                // buffer hs & 1 was last read by step hs - 2's accumulation, issued earlier
+                const uint32_t bc = (hs & 1) * C::BUF_COLS;
+                mm_kk(bc + C::S_OFF, fixA_k, ring_k + (uint64_t)((sa * C::RING_BYTES) >> 4));   // S (S^T)
+                mm_kk(bc + C::DP_OFF, fixB_k, ring_k + (uint64_t)((sb * C::RING_BYTES) >> 4));  // dP (dP^T)
+                commit(&bars->s_full[hs & 1]);
+                if (s == hi - 1) commit(&bars->fix_empty);
+                if (pend && !issue_acc(hs - 1, psa, psb)) break;
+                psa = sa;
+                psb = sb;
+                pend = true;
+                ++hs;
                 rc += 2;
             }
+            if (!ok) break;
+            if (!issue_acc(hs - 1, psa, psb)) break;
+            commit(&bars->acc_done);
         }
         if (!ok && lane == 0) bwd_timeout(p, bars);
         commit(&bars->drain);
@@ -317,14 +339,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp < C::COMPUTE_WARPS) {
         // ---------------------------------------------------------------- compute warpgroups
-        // warpgroup wg owns columns [64 wg, 64 wg + 64) of every step; a warp reaches the
+        // warpgroup wg owns columns [32 wg, 32 wg + 32) of every step; a warp reaches the
         // TMEM lanes of its index within the warpgroup
         const int wg = warp >> 2;
         const int trow = (warp & 3) * 32 + lane;        // row of this thread in the tile
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const float NEG_INF = -__int_as_float(0x7f800000);
         const float LOG2E = 1.4426950408889634f;
-        uint32_t s_phase = 0, uc = 0, colstep = 0;
+        uint32_t hs = 0, uc = 0, colstep = 0;
         bool ok = true;
         auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
@@ -332,130 +353,138 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             if (!r) ok = false;
             return r;
         };
+        // dK/dV pass: per-column LSE (log2 units, warpgroup 0) and D (warpgroup 1) of the
+        // step starting at column c, one value per thread of the first 64 rows
+        const bool stager = trow < C::BC;
+        auto col_value = [&](int bh, int c) -> float {
+            const int col = min(c + trow, p.N - 1);
+            return wg == 0 ? __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E
+                           : __ldg(p.delta + (size_t)bh * p.N + col);
+        };
+        auto col_publish = [&](uint32_t cs, float v) {
+            if (stager) {
+                if (wg == 0) bars->col_lse2[cs & 1][trow] = v;
+                else bars->col_delta[cs & 1][trow] = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->col_ready[cs & 1]));
+        };
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
             const int bh = u / p.nt, t = u - bh * p.nt;
             int lo, hi;
-            bwd_range(p, t, !kDQ, lo, hi);
+            bwd_steps(p, t, !kDQ, lo, hi);
             const int my = t * 128 + trow;              // this thread's row (query or key)
             const bool valid = my < p.N;
-            // dQ pass: per-row LSE and D; dK/dV pass: per-column values come from global below
+            // dQ pass: per-row LSE and D; dK/dV pass: per-column values staged in smem.
+            // A column buffer's previous readers were two steps back: every warp arrives
+            // on col_ready only after finishing the step before the one it publishes for.
             float lse2 = 0.0f, dlt = 0.0f;
             if constexpr (kDQ) {
                 lse2 = valid ? p.lse[(size_t)bh * p.N + my] * LOG2E : 0.0f;
                 dlt = valid ? p.delta[(size_t)bh * p.N + my] : 0.0f;
+            } else {
+                col_publish(colstep, stager ? col_value(bh, lo * C::BC) : 0.0f);
             }
-            for (int jj = lo; jj < hi; ++jj) {
-                const int c0 = jj * 128;                // first column (key / query) of the step
-                const int cb = colstep & 1;
+            // The columns (the other index) the mask allows for this thread's row form one
+            // interval [m_lo, m_hi]: for a query row, keys from i - w (w > 0) or 0 to i
+            // (causal) or i + w (window) or N - 1; for a key row, queries from j (causal) or
+            // j - w (window) or 0, to j + w (window) or N - 1.  One unsigned compare per
+            // element tests it.  A row past N gets some interval: its values stay finite and
+            // are never stored (row r of a product depends on row r of its TMEM operand only).
+            int m_lo, m_hi;
+            if constexpr (kDQ) {
+                m_lo = p.window > 0 ? my - p.window : 0;
+                m_hi = p.causal ? my : (p.window > 0 ? my + p.window : p.N - 1);
+            } else {
+                m_lo = p.causal ? my : (p.window > 0 ? my - p.window : 0);
+                m_hi = p.window > 0 ? my + p.window : p.N - 1;
+            }
+            m_hi = min(m_hi, p.N - 1);
+            const uint32_t m_span = (uint32_t)(m_hi - m_lo);
+            for (int s = lo; s < hi; ++s) {
+                const int c0 = s * C::BC;               // first column (key / query) of the step
+                const int cc = wg * 32;                 // this warpgroup's columns within the step
+                const uint32_t cb = colstep & 1;
+                [[maybe_unused]] float next_col = 0.0f;
                 if constexpr (!kDQ) {
-                    // stage this step's column values (one per thread).  Every warp arrives
-                    // only after finishing the step before, the buffer's previous user was
-                    // two steps back, so once col_ready completes the buffer is consistent.
-                    // warpgroup 0 loads the LSE, warpgroup 1 the D of the 128 columns
-                    const int col = min(c0 + trow, p.N - 1);
-                    if (wg == 0)
-                        bars->col_lse2[cb][trow] = __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E;
-                    else
-                        bars->col_delta[cb][trow] = __ldg(p.delta + (size_t)bh * p.N + col);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&bars->col_ready[cb]));
+                    if (stager && s + 1 < hi) next_col = col_value(bh, c0 + C::BC);   // prefetch
                     if (!wait_all(&bars->col_ready[cb], (colstep >> 1) & 1)) break;
                 }
-                ++colstep;
-                if (!wait_all(&bars->s_full, s_phase)) break;
-                s_phase ^= 1;
+                if (!wait_all(&bars->s_full[hs & 1], (hs >> 1) & 1)) break;
                 tc_fence_after_sync();
-                // P and dS of this thread's row over the warpgroup's 64 columns, 32 at a time;
-                // the mask is evaluated only on tiles that cross the diagonal, a window edge
-                // or the sequence end
+                const uint32_t base = tmem + lane_addr + (hs & 1) * C::BUF_COLS;
+                // P and dS of this thread's row over the warpgroup's 32 columns; the mask is
+                // evaluated only on blocks that cross the diagonal, a window edge or the end
                 auto step = [&](auto masked_tag) {
                     constexpr bool kMasked = decltype(masked_tag)::value;
-                    // The columns (the other index) the mask allows for this thread's row form
-                    // one interval [m_lo, m_hi]: for a query row, keys from max(0, i - w) (w > 0)
-                    // to i (causal) or i + w (window) or N - 1; for a key row, queries from j
-                    // (causal) or j - w (window) or 0, to j + w (window) or N - 1.  One unsigned
-                    // compare per element tests it.  A row past N gets some interval: its
-                    // values stay finite and are never stored (row r of a product depends on
-                    // row r of the TMEM operand only).
-                    int m_lo, m_hi;
-                    if constexpr (kDQ) {
-                        m_lo = p.window > 0 ? my - p.window : 0;
-                        m_hi = p.causal ? my : (p.window > 0 ? my + p.window : p.N - 1);
-                    } else {
-                        m_lo = p.causal ? my : (p.window > 0 ? my - p.window : 0);
-                        m_hi = p.window > 0 ? my + p.window : p.N - 1;
-                    }
-                    m_hi = min(m_hi, p.N - 1);
-                    const uint32_t m_span = (uint32_t)(m_hi - m_lo);
-                    const uint32_t base = tmem + lane_addr;
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32p(base + C::S_OFF + cc, sr);
+                    tmem_ld32p(base + C::DP_OFF + cc, dr);
+                    tmem_wait_ld_only();
+                    reg_fence32(sr);
+                    reg_fence32(dr);
+                    uint32_t pk[16];
+                    [[maybe_unused]] uint32_t pkp[16];
+                    [[maybe_unused]] float4 l4, d4;
 #pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
-                        const int cc = wg * 64 + ch * 32;       // first column of the chunk
-                        uint32_t sr[32], dr[32];
-                        tmem_ld32p(base + C::S_COL + cc, sr);
-                        tmem_ld32p(base + C::DP_COL + cc, dr);
-                        tmem_wait_ld_only();
-                        reg_fence32(sr);
-                        reg_fence32(dr);
-                        uint32_t pk[16];
-                        [[maybe_unused]] uint32_t pkp[16];
-                        [[maybe_unused]] float4 l4, d4;
+                    for (int e = 0; e < 16; ++e) {
+                        if constexpr (!kDQ) {
+                            if ((e & 1) == 0) {   // four columns' LSE and D per vector load
+                                l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][cc + 2 * e]);
+                                d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][cc + 2 * e]);
+                            }
+                        }
+                        float pv[2], dsv[2];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            float l2 = lse2, dl = dlt;
                             if constexpr (!kDQ) {
-                                if ((e & 1) == 0) {   // four columns' LSE and D per vector load
-                                    l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][cc + 2 * e]);
-                                    d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][cc + 2 * e]);
-                                }
+                                l2 = (e & 1) ? (h2 ? l4.w : l4.z) : (h2 ? l4.y : l4.x);
+                                dl = (e & 1) ? (h2 ? d4.w : d4.z) : (h2 ? d4.y : d4.x);
                             }
-                            float pv[2], dsv[2];
-#pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                float l2 = lse2, dl = dlt;
-                                if constexpr (!kDQ) {
-                                    l2 = (e & 1) ? (h2 ? l4.w : l4.z) : (h2 ? l4.y : l4.x);
-                                    dl = (e & 1) ? (h2 ? d4.w : d4.z) : (h2 ? d4.y : d4.x);
-                                }
-                                const float sv = __uint_as_float(sr[2 * e + h2]);
-                                float pr = ex2(fmaf(sv, p.c_log2, -l2));
-                                if constexpr (kMasked) {
-                                    // column c0 + cc + 2e + h2 is allowed iff it lies in [lo, hi]
-                                    const uint32_t off = (uint32_t)(c0 + cc - m_lo) + (uint32_t)(2 * e + h2);
-                                    pr = off <= m_span ? pr : 0.0f;
-                                }
-                                pv[h2] = pr;
-                                dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
+                            const float sv = __uint_as_float(sr[2 * e + h2]);
+                            float pr = ex2(fmaf(sv, p.c_log2, -l2));
+                            if constexpr (kMasked) {
+                                // column c0 + cc + 2e + h2 is allowed iff it lies in [m_lo, m_hi]
+                                const uint32_t off = (uint32_t)(c0 + cc - m_lo) + (uint32_t)(2 * e + h2);
+                                pr = off <= m_span ? pr : 0.0f;
                             }
-                            pk[e] = pack_bf16x2(dsv[0], dsv[1]);
-                            if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
+                            pv[h2] = pr;
+                            dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
                         }
-                        // bf16 pairs: the chunk's 32 columns fill 16 packed TMEM columns at
-                        // 64 wg + 16 ch, inside this warpgroup's own S (dP) columns whose values
-                        // it has already loaded; the other warpgroup's columns are untouched
-                        const uint32_t pc = (uint32_t)(wg * 64 + ch * 16);
-                        if constexpr (kDQ) {
-                            tmem_st16p(base + C::S_COL + pc, pk);             // dS over S
-                        } else {
-                            tmem_st16p(base + C::S_COL + pc, pkp);            // P^T over S^T
-                            tmem_st16p(base + C::DP_COL + pc, pk);            // dS^T over dP^T
-                        }
+                        pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                        if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
+                    }
+                    // bf16 pairs: the 32 columns fill 16 packed TMEM columns at the start of
+                    // this warpgroup's own S (dP) columns, whose values are already loaded
+                    if constexpr (kDQ) {
+                        tmem_st16p(base + C::S_OFF + cc, pk);             // dS over S
+                    } else {
+                        tmem_st16p(base + C::S_OFF + cc, pkp);            // P^T over S^T
+                        tmem_st16p(base + C::DP_OFF + cc, pk);            // dS^T over dP^T
                     }
                 };
-                if (bwd_tile_full(p, kDQ ? t * 128 : c0, kDQ ? c0 : t * 128))
+                if (bwd_block_full(p, kDQ ? t * 128 : c0, kDQ ? 128 : C::BC, kDQ ? c0 : t * 128,
+                                   kDQ ? C::BC : 128))
                     step(std::false_type{});
                 else
                     step(std::true_type{});
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[hs & 1]));
+                ++hs;
+                if constexpr (!kDQ) {
+                    if (s + 1 < hi) col_publish(colstep + 1, next_col);
+                    ++colstep;
+                }
             }
             if (!ok) break;
-            // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16
-            if (!wait_all(&bars->acc_done, uc & 1)) break;
-            tc_fence_after_sync();
+            // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16.
             // dQ pass: each warpgroup writes half of dQ's columns; dK/dV pass: warpgroup 0
             // writes dV, warpgroup 1 dK
+            if (!wait_all(&bars->acc_done, uc & 1)) break;
+            tc_fence_after_sync();
             {
                 const int which = kDQ ? 0 : wg;
                 const float f = kDQ ? p.scale : (which == 0 ? 1.0f : p.scale);
@@ -494,8 +523,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 }
 
 template <int D>
-cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const BwdParams& p, int sm_count, cudaStream_t stream)
+cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cudaStream_t stream)
 {
     using C = BwdCfg<D>;
     const long long rows = (long long)p.BH * p.N;
@@ -510,18 +538,16 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
         return e;
     if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
         return e;
-    kq<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    kq<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.q, m.dout, m.k64, m.v64, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kkv<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+    kkv<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.k, m.v, m.q64, m.dout64, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const BwdParams& p, int d, int sm_count,
-                       cudaStream_t stream)
+cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count, cudaStream_t stream)
 {
-    if (d == 64) return launch_bwd_t<64>(mq, mk, mv, mdo, p, sm_count, stream);
-    if (d == 128) return launch_bwd_t<128>(mq, mk, mv, mdo, p, sm_count, stream);
+    if (d == 64) return launch_bwd_t<64>(m, p, sm_count, stream);
+    if (d == 128) return launch_bwd_t<128>(m, p, sm_count, stream);
     return cudaErrorInvalidValue;
 }
 

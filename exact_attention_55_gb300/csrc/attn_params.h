@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include <cuda.h>
+
 namespace gb300 {
 
 // Status codes written to the device status word (same values as attn_status_t).
@@ -51,6 +53,13 @@ struct BwdParams {
     float c_log2;         // scale * log2(e)
     float scale;
     unsigned long long timeout_ns;
+};
+
+// Tensor maps of the backward pass: 128-row boxes for a unit's fixed tiles, 64-row
+// boxes for the ring tiles of a step.
+struct BwdMaps {
+    CUtensorMap q, k, v, dout;
+    CUtensorMap q64, k64, v64, dout64;
 };
 
 // One decoding step over a paged KV cache (decode.cu).
