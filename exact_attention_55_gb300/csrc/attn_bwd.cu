@@ -22,12 +22,13 @@
 //
 // Software pipeline: S and dP of a step live in one of two TMEM buffers, so the MMA
 // warp issues step h's S and dP before step h-1's accumulation and the tensor pipe
-// computes them while the compute warpgroups turn step h-1 into P and dS.
+// computes them while a compute warpgroup turns step h-1 into P and dS.  The two
+// compute warpgroups ping-pong: warpgroup b takes the steps of buffer b (every other
+// step), so each has two steps' worth of tensor time for its own.
 //
 // Roles per CTA (persistent over units): warps 0-7 compute (two warpgroups, one thread
-// per tile row, each warpgroup 32 of the step's 64 columns), warp 8 streams tiles with
-// TMA through an mbarrier ring, warp 9 issues the tcgen05.mma.  Every wait is bounded
-// and gives up with ATTN_ERR_TIMEOUT.
+// per tile row), warp 8 streams tiles with TMA through an mbarrier ring, warp 9 issues
+// the tcgen05.mma.  Every wait is bounded and gives up with ATTN_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -48,7 +49,7 @@ struct BwdCfg {
     static constexpr int RING_CB = BC * 128;       // one column block of a ring tile
     static constexpr int RING_BYTES = NCB * RING_CB;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = 2048;         // barriers + the staged LSE / D columns
+    static constexpr int BAR_BYTES = 5120;         // barriers + the per-warp LSE / D columns
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * FIX_BYTES) / RING_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
@@ -58,7 +59,7 @@ struct BwdCfg {
     static constexpr int DP_OFF = 64;              // dP (then dS^T in the dK/dV pass)
     static constexpr int ACC_COL = 256;            // dQ, or dV then dK at ACC_COL + D
     static constexpr int TMEM_COLS = 512;
-    static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, 32 columns each
+    static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, one per step buffer
     static constexpr int NUM_THREADS = 320;
     static constexpr int PRODUCER_WARP = 8;
     static constexpr int MMA_WARP = 9;
@@ -71,18 +72,16 @@ struct BwdCfg {
 struct alignas(16) BwdBars {
     uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
     uint64_t ring_full[8], ring_empty[8];
-    uint64_t s_full[2], p_full[2];       // per TMEM step buffer
+    uint64_t s_full[2], p_full[2];       // per TMEM step buffer (and compute warpgroup)
     uint64_t acc_done, acc_empty;
-    uint64_t col_ready[2];               // dK/dV pass: the eight compute warps staged a column set
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    // dK/dV pass: LSE (log2 units) and D of a step's 64 query columns, double-buffered
-    // by step parity and filled by the compute threads themselves
-    alignas(16) float col_lse2[2][64];
-    alignas(16) float col_delta[2][64];
+    // dK/dV pass: each compute warp's copy of the LSE (log2 units, [w][0]) and D ([w][1])
+    // of its current step's 64 query columns
+    alignas(16) float col[8][2][64];
 };
-static_assert(sizeof(BwdBars) <= 2048, "barrier block");
+static_assert(sizeof(BwdBars) <= 5120, "barrier block");
 
 __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
 {
@@ -177,8 +176,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->s_full[b]), 1);
-            mbar_init(smem_u32(&bars->p_full[b]), C::COMPUTE_WARPS);
-            mbar_init(smem_u32(&bars->col_ready[b]), C::COMPUTE_WARPS);
+            mbar_init(smem_u32(&bars->p_full[b]), C::COMPUTE_WARPS / 2);
         }
         mbar_init(smem_u32(&bars->acc_done), 1);
         mbar_init(smem_u32(&bars->acc_empty), C::COMPUTE_WARPS);
@@ -274,14 +272,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 mma_ss_warp<false>(tmem + d_col, a0 + offa, b0 + offb, idesc_kk, kk > 0 ? 1u : 0u);
             }
         };
-        // acc[128 x D] (+)= A (TMEM, 128 x 64 bf16) * B (ring tile as MN-major, K = 64 rows).
-        // A's bf16 pairs for K rows 0-31 sit at a_col + [0, 16), rows 32-63 at
-        // a_col + [32, 48): each compute warpgroup packs over its own 32 columns.
+        // acc[128 x D] (+)= A (TMEM, 128 x 64 bf16 as 32 columns of pairs at a_col) * B (ring
+        // tile as MN-major, K = 64 rows)
         auto mm_acc = [&](uint32_t acc_col, uint32_t a_col, uint64_t bmn, bool accumulate) {
 #pragma unroll
             for (int kk = 0; kk < C::BC / 16; ++kk)
-                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + (kk / 2) * 32 + (kk % 2) * 8,
-                                   bmn + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
+                mma_ts_warp<false>(tmem + acc_col, tmem + a_col + kk * 8, bmn + ((kk * 16 * 128) >> 4),
+                                   idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
             int lo, hi;
@@ -339,13 +336,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp < C::COMPUTE_WARPS) {
         // ---------------------------------------------------------------- compute warpgroups
-        // warpgroup wg owns columns [32 wg, 32 wg + 32) of every step; a warp reaches the
-        // TMEM lanes of its index within the warpgroup
+        // warpgroup wg takes the steps whose global index h has h & 1 == wg (TMEM buffer
+        // wg); a warp reaches the TMEM lanes of its index within the warpgroup
         const int wg = warp >> 2;
         const int trow = (warp & 3) * 32 + lane;        // row of this thread in the tile
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t buf = tmem + lane_addr + (uint32_t)wg * C::BUF_COLS;
         const float LOG2E = 1.4426950408889634f;
-        uint32_t hs = 0, uc = 0, colstep = 0;
+        uint32_t h = 0, uc = 0;
         bool ok = true;
         auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
@@ -353,21 +351,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             if (!r) ok = false;
             return r;
         };
-        // dK/dV pass: per-column LSE (log2 units, warpgroup 0) and D (warpgroup 1) of the
-        // step starting at column c, one value per thread of the first 64 rows
-        const bool stager = trow < C::BC;
-        auto col_value = [&](int bh, int c) -> float {
-            const int col = min(c + trow, p.N - 1);
-            return wg == 0 ? __ldg(p.lse + (size_t)bh * p.N + col) * LOG2E
-                           : __ldg(p.delta + (size_t)bh * p.N + col);
-        };
-        auto col_publish = [&](uint32_t cs, float v) {
-            if (stager) {
-                if (wg == 0) bars->col_lse2[cs & 1][trow] = v;
-                else bars->col_delta[cs & 1][trow] = v;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars->col_ready[cs & 1]));
+        // dK/dV pass: lane l holds the LSE (log2 units) and D of columns c + 2l, c + 2l + 1
+        // of a step; each warp keeps its own copy in shared memory while it works on it
+        float* my_lse2 = bars->col[warp][0];
+        float* my_delta = bars->col[warp][1];
+        auto col_load = [&](int bh, int c, float2& l2v, float2& dv) {
+            const size_t base = (size_t)bh * p.N;
+            const int c0 = min(c + 2 * lane, p.N - 1), c1 = min(c + 2 * lane + 1, p.N - 1);
+            l2v = make_float2(__ldg(p.lse + base + c0) * LOG2E, __ldg(p.lse + base + c1) * LOG2E);
+            dv = make_float2(__ldg(p.delta + base + c0), __ldg(p.delta + base + c1));
         };
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
             const int bh = u / p.nt, t = u - bh * p.nt;
@@ -375,15 +367,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             bwd_steps(p, t, !kDQ, lo, hi);
             const int my = t * 128 + trow;              // this thread's row (query or key)
             const bool valid = my < p.N;
-            // dQ pass: per-row LSE and D; dK/dV pass: per-column values staged in smem.
-            // A column buffer's previous readers were two steps back: every warp arrives
-            // on col_ready only after finishing the step before the one it publishes for.
-            float lse2 = 0.0f, dlt = 0.0f;
+            float lse2 = 0.0f, dlt = 0.0f;              // dQ pass: per-row LSE and D
             if constexpr (kDQ) {
                 lse2 = valid ? p.lse[(size_t)bh * p.N + my] * LOG2E : 0.0f;
                 dlt = valid ? p.delta[(size_t)bh * p.N + my] : 0.0f;
-            } else {
-                col_publish(colstep, stager ? col_value(bh, lo * C::BC) : 0.0f);
             }
             // The columns (the other index) the mask allows for this thread's row form one
             // interval [m_lo, m_hi]: for a query row, keys from i - w (w > 0) or 0 to i
@@ -401,67 +388,81 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             }
             m_hi = min(m_hi, p.N - 1);
             const uint32_t m_span = (uint32_t)(m_hi - m_lo);
-            for (int s = lo; s < hi; ++s) {
+            const uint32_t h0 = h;                      // global index of step lo
+            h = h0 + (uint32_t)(hi - lo);
+            int s = lo + (int)((h0 ^ (uint32_t)wg) & 1u);   // this warpgroup's first step
+            [[maybe_unused]] float2 nl2 = make_float2(0.f, 0.f), nd = nl2;
+            if constexpr (!kDQ) {
+                if (s < hi) col_load(bh, s * C::BC, nl2, nd);
+            }
+            for (; s < hi; s += 2) {
+                const uint32_t hh = h0 + (uint32_t)(s - lo);
                 const int c0 = s * C::BC;               // first column (key / query) of the step
-                const int cc = wg * 32;                 // this warpgroup's columns within the step
-                const uint32_t cb = colstep & 1;
-                [[maybe_unused]] float next_col = 0.0f;
                 if constexpr (!kDQ) {
-                    if (stager && s + 1 < hi) next_col = col_value(bh, c0 + C::BC);   // prefetch
-                    if (!wait_all(&bars->col_ready[cb], (colstep >> 1) & 1)) break;
+                    // publish this step's column values to the warp's copy, then prefetch
+                    // the warpgroup's next step (two on) into registers
+                    __syncwarp();                       // the previous step's reads are done
+                    *reinterpret_cast<float2*>(my_lse2 + 2 * lane) = nl2;
+                    *reinterpret_cast<float2*>(my_delta + 2 * lane) = nd;
+                    __syncwarp();
+                    if (s + 2 < hi) col_load(bh, c0 + 2 * C::BC, nl2, nd);
                 }
-                if (!wait_all(&bars->s_full[hs & 1], (hs >> 1) & 1)) break;
+                if (!wait_all(&bars->s_full[wg], (hh >> 1) & 1)) break;
                 tc_fence_after_sync();
-                const uint32_t base = tmem + lane_addr + (hs & 1) * C::BUF_COLS;
-                // P and dS of this thread's row over the warpgroup's 32 columns; the mask is
-                // evaluated only on blocks that cross the diagonal, a window edge or the end
+                // P and dS of this thread's row over the step's 64 columns, 32 at a time; the
+                // mask is evaluated only on blocks that cross the diagonal, a window edge or
+                // the sequence end
                 auto step = [&](auto masked_tag) {
                     constexpr bool kMasked = decltype(masked_tag)::value;
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32p(base + C::S_OFF + cc, sr);
-                    tmem_ld32p(base + C::DP_OFF + cc, dr);
-                    tmem_wait_ld_only();
-                    reg_fence32(sr);
-                    reg_fence32(dr);
-                    uint32_t pk[16];
-                    [[maybe_unused]] uint32_t pkp[16];
-                    [[maybe_unused]] float4 l4, d4;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        if constexpr (!kDQ) {
-                            if ((e & 1) == 0) {   // four columns' LSE and D per vector load
-                                l4 = *reinterpret_cast<const float4*>(&bars->col_lse2[cb][cc + 2 * e]);
-                                d4 = *reinterpret_cast<const float4*>(&bars->col_delta[cb][cc + 2 * e]);
-                            }
-                        }
-                        float pv[2], dsv[2];
+                    for (int ch = 0; ch < 2; ++ch) {
+                        const int cc = ch * 32;
+                        uint32_t sr[32], dr[32];
+                        tmem_ld32p(buf + C::S_OFF + cc, sr);
+                        tmem_ld32p(buf + C::DP_OFF + cc, dr);
+                        tmem_wait_ld_only();
+                        reg_fence32(sr);
+                        reg_fence32(dr);
+                        uint32_t pk[16];
+                        [[maybe_unused]] uint32_t pkp[16];
+                        [[maybe_unused]] float4 l4, d4;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            float l2 = lse2, dl = dlt;
+                        for (int e = 0; e < 16; ++e) {
                             if constexpr (!kDQ) {
-                                l2 = (e & 1) ? (h2 ? l4.w : l4.z) : (h2 ? l4.y : l4.x);
-                                dl = (e & 1) ? (h2 ? d4.w : d4.z) : (h2 ? d4.y : d4.x);
+                                if ((e & 1) == 0) {   // four columns' LSE and D per vector load
+                                    l4 = *reinterpret_cast<const float4*>(my_lse2 + cc + 2 * e);
+                                    d4 = *reinterpret_cast<const float4*>(my_delta + cc + 2 * e);
+                                }
                             }
-                            const float sv = __uint_as_float(sr[2 * e + h2]);
-                            float pr = ex2(fmaf(sv, p.c_log2, -l2));
-                            if constexpr (kMasked) {
-                                // column c0 + cc + 2e + h2 is allowed iff it lies in [m_lo, m_hi]
-                                const uint32_t off = (uint32_t)(c0 + cc - m_lo) + (uint32_t)(2 * e + h2);
-                                pr = off <= m_span ? pr : 0.0f;
+                            float pv[2], dsv[2];
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                float l2 = lse2, dl = dlt;
+                                if constexpr (!kDQ) {
+                                    l2 = (e & 1) ? (h2 ? l4.w : l4.z) : (h2 ? l4.y : l4.x);
+                                    dl = (e & 1) ? (h2 ? d4.w : d4.z) : (h2 ? d4.y : d4.x);
+                                }
+                                const float sv = __uint_as_float(sr[2 * e + h2]);
+                                float pr = ex2(fmaf(sv, p.c_log2, -l2));
+                                if constexpr (kMasked) {
+                                    // column c0 + cc + 2e + h2 is allowed iff it lies in [m_lo, m_hi]
+                                    const uint32_t off = (uint32_t)(c0 + cc - m_lo) + (uint32_t)(2 * e + h2);
+                                    pr = off <= m_span ? pr : 0.0f;
+                                }
+                                pv[h2] = pr;
+                                dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
                             }
-                            pv[h2] = pr;
-                            dsv[h2] = pr * (__uint_as_float(dr[2 * e + h2]) - dl);
+                            pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                            if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
                         }
-                        pk[e] = pack_bf16x2(dsv[0], dsv[1]);
-                        if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
-                    }
-                    // bf16 pairs: the 32 columns fill 16 packed TMEM columns at the start of
-                    // this warpgroup's own S (dP) columns, whose values are already loaded
-                    if constexpr (kDQ) {
-                        tmem_st16p(base + C::S_OFF + cc, pk);             // dS over S
-                    } else {
-                        tmem_st16p(base + C::S_OFF + cc, pkp);            // P^T over S^T
-                        tmem_st16p(base + C::DP_OFF + cc, pk);            // dS^T over dP^T
+                        // bf16 pairs: chunk ch fills packed TMEM columns [16 ch, 16 ch + 16) of
+                        // the buffer's S (dP) columns, which this thread has already loaded
+                        if constexpr (kDQ) {
+                            tmem_st16p(buf + C::S_OFF + ch * 16, pk);             // dS over S
+                        } else {
+                            tmem_st16p(buf + C::S_OFF + ch * 16, pkp);            // P^T over S^T
+                            tmem_st16p(buf + C::DP_OFF + ch * 16, pk);            // dS^T over dP^T
+                        }
                     }
                 };
                 if (bwd_block_full(p, kDQ ? t * 128 : c0, kDQ ? 128 : C::BC, kDQ ? c0 : t * 128,
@@ -472,12 +473,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[hs & 1]));
-                ++hs;
-                if constexpr (!kDQ) {
-                    if (s + 1 < hi) col_publish(colstep + 1, next_col);
-                    ++colstep;
-                }
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[wg]));
             }
             if (!ok) break;
             // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16.
