@@ -28,7 +28,9 @@
 //
 // Roles per CTA (persistent over units): warps 0-7 compute (two warpgroups, one thread
 // per tile row), warp 8 streams tiles with TMA through an mbarrier ring, warp 9 issues
-// the tcgen05.mma.  Every wait is bounded and gives up with ATTN_ERR_TIMEOUT.
+// the tcgen05.mma, warps 10-11 only complete the control warpgroup (registers move from
+// it to the compute warpgroups).  Every wait is bounded and gives up with
+// ATTN_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -60,9 +62,14 @@ struct BwdCfg {
     static constexpr int ACC_COL = 256;            // dQ, or dV then dK at ACC_COL + D
     static constexpr int TMEM_COLS = 512;
     static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, one per step buffer
-    static constexpr int NUM_THREADS = 320;
+    static constexpr int NUM_THREADS = 384;        // + one control warpgroup (2 spare warps)
     static constexpr int PRODUCER_WARP = 8;
     static constexpr int MMA_WARP = 9;
+    // Register split: the compute warpgroups grow to REG_COMPUTE, the control warpgroup
+    // shrinks to REG_CONTROL; needs REG_POOL <= registers per thread at launch * NUM_THREADS.
+    static constexpr int REG_COMPUTE = 208;
+    static constexpr int REG_CONTROL = 88;
+    static constexpr int REG_POOL = 256 * REG_COMPUTE + 128 * REG_CONTROL;
     static_assert(D == 64 || D == 128, "backward head dim");
     static_assert(2 * BUF_COLS <= ACC_COL && ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
     static_assert(NSLOT >= 6, "ring too small");
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == C::PRODUCER_WARP) {
+        regs_decrease<C::REG_CONTROL>();
         if (lane == 0) {
             const uint64_t pol_fix = l2_policy_evict_first();
             const uint64_t pol_ring = l2_policy_evict_last();
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             }
         }
     } else if (warp == C::MMA_WARP) {
+        regs_decrease<C::REG_CONTROL>();
         constexpr uint32_t idesc_kk = idesc_f32acc(1, 0, 128, C::BC);  // bf16, both K-major, N = 64
         constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);     // B MN-major, N = D
         const uint64_t fixA_k = sdesc_sw128(smem_u32(fix), 16, 1024);
@@ -338,6 +347,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         // ---------------------------------------------------------------- compute warpgroups
         // warpgroup wg takes the steps whose global index h has h & 1 == wg (TMEM buffer
         // wg); a warp reaches the TMEM lanes of its index within the warpgroup
+        regs_increase<C::REG_COMPUTE>();
         const int wg = warp >> 2;
         const int trow = (warp & 3) * 32 + lane;        // row of this thread in the tile
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
@@ -414,15 +424,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 // the sequence end
                 auto step = [&](auto masked_tag) {
                     constexpr bool kMasked = decltype(masked_tag)::value;
+                    uint32_t sra[64], dra[64];              // the step's S and dP row, one wait
+                    tmem_ld32p(buf + C::S_OFF, sra);
+                    tmem_ld32p(buf + C::S_OFF + 32, sra + 32);
+                    tmem_ld32p(buf + C::DP_OFF, dra);
+                    tmem_ld32p(buf + C::DP_OFF + 32, dra + 32);
+                    tmem_wait_ld_only();
+                    reg_fence32(sra);
+                    reg_fence32(sra + 32);
+                    reg_fence32(dra);
+                    reg_fence32(dra + 32);
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         const int cc = ch * 32;
-                        uint32_t sr[32], dr[32];
-                        tmem_ld32p(buf + C::S_OFF + cc, sr);
-                        tmem_ld32p(buf + C::DP_OFF + cc, dr);
-                        tmem_wait_ld_only();
-                        reg_fence32(sr);
-                        reg_fence32(dr);
+                        const uint32_t* sr = sra + cc;
+                        const uint32_t* dr = dra + cc;
                         uint32_t pk[16];
                         [[maybe_unused]] uint32_t pkp[16];
                         [[maybe_unused]] float4 l4, d4;
@@ -456,7 +472,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                             if constexpr (!kDQ) pkp[e] = pack_bf16x2(pv[0], pv[1]);
                         }
                         // bf16 pairs: chunk ch fills packed TMEM columns [16 ch, 16 ch + 16) of
-                        // the buffer's S (dP) columns, which this thread has already loaded
+                        // the buffer's S (dP) columns, already loaded above
                         if constexpr (kDQ) {
                             tmem_st16p(buf + C::S_OFF + ch * 16, pk);             // dS over S
                         } else {
@@ -511,6 +527,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
         }
         if (!ok) bwd_timeout(p, bars);
+    } else {
+        regs_decrease<C::REG_CONTROL>();                // spare warps of the control warpgroup
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -534,6 +552,12 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cud
         return e;
     if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
         return e;
+    // setmaxnreg.inc would wait forever if the launch pool were smaller than the split
+    for (const void* f : {reinterpret_cast<const void*>(kq), reinterpret_cast<const void*>(kkv)}) {
+        cudaFuncAttributes attr;
+        if ((e = cudaFuncGetAttributes(&attr, f)) != cudaSuccess) return e;
+        if (attr.numRegs * C::NUM_THREADS < C::REG_POOL) return cudaErrorInvalidConfiguration;
+    }
     kq<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.q, m.dout, m.k64, m.v64, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kkv<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.k, m.v, m.q64, m.dout64, p);
