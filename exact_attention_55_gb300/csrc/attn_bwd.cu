@@ -5,10 +5,11 @@
 // normalised):
 //     D_i = dO_i . O_i,   dP = dO V^T,   dS = P * (dP - D),
 //     dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO.
-// The pages name the backward pass only as what follows the forward ("FlashAttention
-// V3：优化框架吞吐量的关键技术实践" §1.1; "大模型加速-核心网络算子-Flash Attention V3"
-// §2.3 speaks of the forward pass); the formulas are the chain rule through the
-// forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
+// The pages name the backward pass only in passing ("FlashAttention V3：优化框架吞吐量
+// 的关键技术实践" §2.3.2: micro-batches' forward and backward passes overlapped in
+// pipeline training, and its introduction: training as well as inference; "大模型加速-
+// 核心网络算子-Flash Attention V3" §2.3-2.4 call the kernel they describe the forward
+// pass); the formulas are the chain rule through the forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
 //   bwd_dot_kernel          D_i, one warp per row;
 //   bwd_kernel<D, true>     (dQ pass) per 128-row query tile, in steps of 64 keys:
 //                           S = Q K_j^T and dP = dO V_j^T into TMEM, the compute

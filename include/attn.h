@@ -67,7 +67,8 @@ attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o
 /*
  * attn_bwd_bf16 -- backward pass of attn_fwd_bf16: dQ, dK, dV for an upstream dO.
  *
- * The step after the forward pass ([YT] §1.1; [JJ] §2.3 names the forward pass).
+ * The backward pass the pages mention for training ([YT] §2.3.2 流水线并行: forward and
+ * backward of micro-batches overlapped; [JJ] §2.3-2.4 call their kernel the forward pass).
  * With P = exp(scale * Q K^T + mask - LSE) (the forward's LSE, so P is normalised):
  *     D_i = dO_i . O_i,  dP = dO V^T,  dS = P * (dP - D),
  *     dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO.

@@ -30,8 +30,9 @@ Functions and the passage each follows:
                              §1.1 可变序列长度): each sequence attends only within
                              itself, masks relative to its own first token
   attn_bwd_f64               gradients of the forward pass (the backward pass the pages
-                             list as the next step after the forward, [YT] §1.1 and
-                             [JJ] §2.3 "forward pass"): dQ, dK, dV of sum(dO * O)
+                             mention for training: [YT] §2.3.2 流水线并行, forward and
+                             backward of micro-batches; [JJ] §2.3-2.4 call their
+                             kernel the forward pass): dQ, dK, dV of sum(dO * O)
   attn_decode_paged_f64      a decoding step against a paged KV cache ([JJ] §3 总结:
                              tokens generated one at a time over cached K/V; [WGC]
                              §局限性与后续方向 item 2: PagedAttention KV-cache management)
