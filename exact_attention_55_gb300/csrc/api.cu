@@ -511,7 +511,7 @@ extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void*
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (workspace_bytes < (size_t)BH * N * sizeof(float)) return ATTN_ERR_INVALID_ARG;
     const long long nt = (N + 127) / 128;
-    if (BH * nt > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (BH * 2 * ((nt + 1) / 2) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;  // sub-units fit an int
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
         !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
         !aligned(lse, 4) || !aligned(workspace, 4))

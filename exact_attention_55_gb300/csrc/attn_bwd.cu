@@ -121,6 +121,26 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_ti
     hi = min(2 * hi, (p.N + 63) / 64);
 }
 
+// Work order.  A pass's units are the 128-row tiles t of every head; under a causal mask
+// tile t of the dQ pass meets t + 1 key tiles and tile t of the dK/dV pass nt - t query
+// tiles, so units differ in cost and a round-robin over them leaves the busiest CTA ~12 %
+// above the mean.  Units are therefore handed out in complementary pairs (nt - 1 - k, k)
+// whose costs add up to the same nt + 1 tiles for every k; a CTA takes both halves of a
+// pair, pairs go round-robin, and pairs of one head are adjacent so CTAs that run at the
+// same time share that head's operands in L2.  Sub-unit s is half (s & 1) of pair s >> 1;
+// the middle tile of an odd tile count appears once.
+__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, int& bh, int& t)
+{
+    const int npair = (p.nt + 1) >> 1;
+    const int pair = s >> 1;
+    bh = pair / npair;
+    const int k = pair - bh * npair;
+    t = (s & 1) ? k : p.nt - 1 - k;
+    return !((s & 1) && k == p.nt - 1 - k);
+}
+
+__device__ __forceinline__ int bwd_next(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
+
 // True when every (query, key) pair of the block of queries [q0, q0 + nq) and keys
 // [k0, k0 + nk) lies inside the sequence and is allowed by the mask, so the step needs
 // no per-element test: causal needs the last key at or before the first query, a window
@@ -173,7 +193,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
     BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::RING_BYTES);
     const volatile int* abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = p.BH * p.nt;
+    const int nsub = 2 * ((p.nt + 1) >> 1) * p.BH;   // sub-units (see bwd_unit)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->fix_full), 1);
@@ -208,8 +228,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             const uint64_t pol_ring = l2_policy_evict_last();
             uint32_t rc = 0, uc = 0, armed = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-                const int bh = u / p.nt, t = u - bh * p.nt;
+            for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+                int bh, t;
+                if (!bwd_unit(p, su, bh, t)) continue;
                 int lo, hi;
                 bwd_steps(p, t, !kDQ, lo, hi);
                 if (!mbar_wait(smem_u32(&bars->fix_empty), (uc & 1) ^ 1, abort_flag, p.timeout_ns)) {
@@ -244,6 +265,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                         ++rc;
                     }
                 }
+                ++uc;
             }
             if (!ok) {
                 bwd_timeout(p, bars);
@@ -290,9 +312,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 mma_ts_warp<false>(tmem + acc_col, tmem + a_col + kk * 8, bmn + ((kk * 16 * 128) >> 4),
                                    idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+            int bh, t;
+            if (!bwd_unit(p, su, bh, t)) continue;
             int lo, hi;
-            bwd_steps(p, u % p.nt, !kDQ, lo, hi);
+            bwd_steps(p, t, !kDQ, lo, hi);
             if (!wait(&bars->fix_full, uc & 1)) break;
             tc_fence_after_sync();
             bool acc_started = false;
@@ -339,6 +363,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             if (!ok) break;
             if (!issue_acc(hs - 1, psa, psb)) break;
             commit(&bars->acc_done);
+            ++uc;
         }
         if (!ok && lane == 0) bwd_timeout(p, bars);
         commit(&bars->drain);
@@ -372,8 +397,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             l2v = make_float2(__ldg(p.lse + base + c0) * LOG2E, __ldg(p.lse + base + c1) * LOG2E);
             dv = make_float2(__ldg(p.delta + base + c0), __ldg(p.delta + base + c1));
         };
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-            const int bh = u / p.nt, t = u - bh * p.nt;
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+            int bh, t;
+            if (!bwd_unit(p, su, bh, t)) continue;
             int lo, hi;
             bwd_steps(p, t, !kDQ, lo, hi);
             const int my = t * 128 + trow;              // this thread's row (query or key)
@@ -526,6 +552,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty));
+            ++uc;
         }
         if (!ok) bwd_timeout(p, bars);
     } else {
@@ -545,8 +572,8 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cud
     bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int units = p.BH * p.nt;
-    const int grid = units < sm_count ? units : sm_count;
+    const int pairs = ((p.nt + 1) >> 1) * p.BH;     // units go out in pairs (bwd_unit)
+    const int grid = pairs < sm_count ? pairs : sm_count;
     auto kq = bwd_kernel<D, true>;
     auto kkv = bwd_kernel<D, false>;
     if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
