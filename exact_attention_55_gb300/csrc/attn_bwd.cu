@@ -42,25 +42,29 @@
 
 namespace gb300 {
 
-template <int D>
+template <int D, bool kDQ>
 struct BwdCfg {
     static constexpr int BT = 128;                 // rows of a unit's tile (query or key)
-    static constexpr int BC = 64;                  // columns of a step (the other index)
+    static constexpr int BC = kDQ ? 128 : 64;      // columns of a step (the other index)
     static constexpr int NCB = D / 64;             // 128-byte column blocks of a bf16 row
     static constexpr int FIX_CB = BT * 128;        // one column block of a fixed tile
     static constexpr int FIX_BYTES = NCB * FIX_CB;
     static constexpr int RING_CB = BC * 128;       // one column block of a ring tile
     static constexpr int RING_BYTES = NCB * RING_CB;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = 5120;         // barriers + the per-warp LSE / D columns
+    static constexpr int BAR_BYTES = kDQ ? 512 : 512 + 4096;   // barriers (+ dK/dV: per-warp LSE / D)
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * FIX_BYTES) / RING_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
     static constexpr int SMEM_BYTES = ALIGN_SLACK + 2 * FIX_BYTES + NSLOT * RING_BYTES + BAR_BYTES;
-    static constexpr int BUF_COLS = 128;           // TMEM columns of a step buffer
-    static constexpr int S_OFF = 0;                // S (then dS, or P^T) of the step
-    static constexpr int DP_OFF = 64;              // dP (then dS^T in the dK/dV pass)
-    static constexpr int ACC_COL = 256;            // dQ, or dV then dK at ACC_COL + D
+    // TMEM.  dQ pass: S of step h in buffer h & 1 at 128 (h & 1) (then dS, packed), dP at
+    // DQ_DP_COL, dQ at ACC_COL.  dK/dV pass: step buffer h & 1 at 128 (h & 1) holds S^T at
+    // +S_OFF (then P^T) and dP^T at +DP_OFF (then dS^T); dV at ACC_COL, dK at ACC_COL + D.
+    static constexpr int BUF_COLS = 128;
+    static constexpr int S_OFF = 0;
+    static constexpr int DP_OFF = 64;
+    static constexpr int DQ_DP_COL = 256;
+    static constexpr int ACC_COL = kDQ ? 384 : 256;
     static constexpr int TMEM_COLS = 512;
     static constexpr int COMPUTE_WARPS = 8;        // two warpgroups, one per step buffer
     static constexpr int NUM_THREADS = 384;        // + one control warpgroup (2 spare warps)
@@ -72,24 +76,25 @@ struct BwdCfg {
     static constexpr int REG_CONTROL = 88;
     static constexpr int REG_POOL = 256 * REG_COMPUTE + 128 * REG_CONTROL;
     static_assert(D == 64 || D == 128, "backward head dim");
-    static_assert(2 * BUF_COLS <= ACC_COL && ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
-    static_assert(NSLOT >= 6, "ring too small");
+    static_assert(kDQ ? ACC_COL + D <= TMEM_COLS : ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
+    static_assert(NSLOT >= (kDQ ? 5 : 6), "ring too small");
     static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
 };
 
 struct alignas(16) BwdBars {
     uint64_t fix_full, fix_empty;        // the unit's two fixed tiles
     uint64_t ring_full[8], ring_empty[8];
-    uint64_t s_full[2], p_full[2];       // per TMEM step buffer (and compute warpgroup)
+    uint64_t s_full[2], p_full[2];       // dK/dV: per TMEM step buffer (and compute warpgroup);
+                                         // dQ: [0] only, one phase per step
+    uint64_t dp_free;                    // dQ: the compute warps have read the step's dP
     uint64_t acc_done, acc_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    // dK/dV pass: each compute warp's copy of the LSE (log2 units, [w][0]) and D ([w][1])
-    // of its current step's 64 query columns
-    alignas(16) float col[8][2][64];
 };
-static_assert(sizeof(BwdBars) <= 5120, "barrier block");
+static_assert(sizeof(BwdBars) <= 512, "barrier block");
+// dK/dV pass: after the barriers, each compute warp's copy of the LSE (log2 units, [w][0])
+// and D ([w][1]) of its current step's 64 query columns: float [8][2][64].
 
 __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
 {
@@ -97,11 +102,11 @@ __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
 }
 
-// Steps (64-column blocks of the other operand) that tile t (rows [128 t, 128 t + 128))
-// meets under the mask: for a query tile, the key blocks [lo, hi); for a key tile
-// (transposed), the query blocks.  Computed on 128-column tiles, then split in two and
-// cut at the sequence end.
-__device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_tile, int& lo, int& hi)
+// Steps (blocks of `bc` columns of the other operand, bc = 128 or 64) that tile t (rows
+// [128 t, 128 t + 128)) meets under the mask: for a query tile, the key blocks [lo, hi);
+// for a key tile (transposed), the query blocks.  Computed on 128-column tiles, then (bc
+// = 64) split in two and cut at the sequence end.
+__device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_tile, int bc, int& lo, int& hi)
 {
     const int a = t * 128, last = min(p.N, a + 128) - 1;
     lo = 0;
@@ -117,8 +122,10 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_ti
         if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
     }
     if (lo >= hi) hi = lo + 1;  // never empty (cannot happen for the masks above)
-    lo *= 2;
-    hi = min(2 * hi, (p.N + 63) / 64);
+    if (bc == 64) {
+        lo *= 2;
+        hi = min(2 * hi, (p.N + 63) / 64);
+    }
 }
 
 // Work order.  A pass's units are the 128-row tiles t of every head; under a causal mask
@@ -176,15 +183,16 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const BwdParams p)
 }
 
 // One pass.  `kDQ` selects it: the dQ pass's unit is a query tile (fixed tiles Q, dO;
-// ring K, V), the dK/dV pass's unit is a key tile (fixed tiles K, V; ring Q, dO).  The
-// fixed maps have 128-row boxes, the ring maps 64-row boxes.
+// ring V then K of each 128-key step, 128-row boxes), the dK/dV pass's unit is a key tile
+// (fixed tiles K, V; ring Q then dO of each 64-query step, 64-row boxes).  The fixed maps
+// have 128-row boxes.
 template <int D, bool kDQ>
-__global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmFixA, const __grid_constant__ CUtensorMap tmFixB,
                const __grid_constant__ CUtensorMap tmRingA, const __grid_constant__ CUtensorMap tmRingB,
                const BwdParams p)
 {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, kDQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -204,8 +212,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->s_full[b]), 1);
-            mbar_init(smem_u32(&bars->p_full[b]), C::COMPUTE_WARPS / 2);
+            // dQ pass: all eight compute warps arrive per step; dK/dV: one warpgroup
+            mbar_init(smem_u32(&bars->p_full[b]), kDQ ? C::COMPUTE_WARPS : C::COMPUTE_WARPS / 2);
         }
+        mbar_init(smem_u32(&bars->dp_free), C::COMPUTE_WARPS);
         mbar_init(smem_u32(&bars->acc_done), 1);
         mbar_init(smem_u32(&bars->acc_empty), C::COMPUTE_WARPS);
         mbar_init(smem_u32(&bars->drain), 1);
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 int bh, t;
                 if (!bwd_unit(p, su, bh, t)) continue;
                 int lo, hi;
-                bwd_steps(p, t, !kDQ, lo, hi);
+                bwd_steps(p, t, !kDQ, C::BC, lo, hi);
                 if (!mbar_wait(smem_u32(&bars->fix_empty), (uc & 1) ^ 1, abort_flag, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -257,7 +267,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                         }
                         const uint32_t rb = smem_u32(&bars->ring_full[slot]);
                         mbar_arrive_expect_tx(rb, C::RING_BYTES);
-                        const CUtensorMap* map = which == 0 ? &tmRingA : &tmRingB;
+                        // dQ pass: V_j then K_j; dK/dV pass: Q_i then dO_i
+                        const CUtensorMap* map = (which == 0) == kDQ ? &tmRingB : &tmRingA;
 #pragma unroll
                         for (int cb = 0; cb < C::NCB; ++cb)
                             tma_load_3d(smem_u32(ring + slot * C::RING_BYTES + cb * C::RING_CB), map, rb,
@@ -278,6 +289,113 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             }
         }
     } else if (warp == C::MMA_WARP) {
+      if constexpr (kDQ) {
+        // ---------------------------------------------------------------- MMA, dQ pass
+        // Step j (128 keys): S(j) = Q K_j^T into S buffer j & 1, dP(j) = dO V_j^T into the
+        // dP columns, then dQ += dS(j) K_j.  Order per step: dP(j) once the compute warps
+        // have read dP(j-1); the accumulation of step j-1; S(j+1) into the other S buffer.
+        // The tensor core thus computes dP(j) while step j-1's ALU work is still running,
+        // and S(j+1) while step j's is.  Ring tiles: V_j then K_j of every step.
+        regs_decrease<C::REG_CONTROL>();
+        constexpr uint32_t idesc_s = idesc_f32acc(1, 0, 128, 128);   // bf16, both K-major, N = 128
+        constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);    // B MN-major, N = D
+        const uint64_t fixA_k = sdesc_sw128(smem_u32(fix), 16, 1024);                    // Q
+        const uint64_t fixB_k = sdesc_sw128(smem_u32(fix + C::FIX_BYTES), 16, 1024);     // dO
+        const uint64_t ring_k = sdesc_sw128(smem_u32(ring), 16, 1024);
+        const uint64_t ring_mn = sdesc_sw128(smem_u32(ring), C::RING_CB, 1024);
+        uint32_t rc = 0, uc = 0, hs = 0;
+        bool ok = true;
+        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = ok && mbar_wait(smem_u32(bar), parity, abort_flag, p.timeout_ns);
+            r = __all_sync(0xffffffffu, r);
+            if (!r) ok = false;
+            return r;
+        };
+        auto commit = [&](uint64_t* bar) { mma_commit_warp(smem_u32(bar)); };
+        auto slot = [&](uint32_t n) { return n % C::NSLOT; };
+        auto full = [&](uint32_t n) -> bool { return wait(&bars->ring_full[n % C::NSLOT], (n / C::NSLOT) & 1); };
+        // D[128 x 128] = A[128 x D] (fixed tile) B[128 x D]^T (ring tile in slot sl), K = D
+        auto mm_kk = [&](uint32_t d_col, uint64_t a0, uint32_t sl) {
+            const uint64_t b0 = ring_k + (uint64_t)((sl * C::RING_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int byte = kk * 32;
+                const uint32_t offa = ((byte / 128) * C::FIX_CB + (byte % 128)) >> 4;
+                const uint32_t offb = ((byte / 128) * C::RING_CB + (byte % 128)) >> 4;
+                mma_ss_warp<false>(tmem + d_col, a0 + offa, b0 + offb, idesc_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // dQ (+)= dS (TMEM: bf16 pairs of keys 0-63 at a + [0, 32), keys 64-127 at
+        // a + [64, 96), one run per compute warpgroup) * K_j (slot sl as MN-major, K = 128)
+        auto mm_acc = [&](uint32_t a_col, uint32_t sl, bool accumulate) {
+            const uint64_t b0 = ring_mn + (uint64_t)((sl * C::RING_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::BC / 16; ++kk)
+                mma_ts_warp<false>(tmem + C::ACC_COL, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
+                                   b0 + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
+        };
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+            int bh, t;
+            if (!bwd_unit(p, su, bh, t)) continue;
+            (void)bh;
+            int lo, hi;
+            bwd_steps(p, t, false, C::BC, lo, hi);
+            const uint32_t r0 = rc, h0 = hs;            // tiles: V_j at r0 + 2(j-lo), K_j next
+            if (!wait(&bars->fix_full, uc & 1)) break;
+            tc_fence_after_sync();
+            if (!full(r0 + 1)) break;                   // K_lo
+            tc_fence_after_sync();
+            mm_kk((h0 & 1) * C::BUF_COLS, fixA_k, slot(r0 + 1));          // S(lo)
+            bool acc_started = false;
+            for (int j = lo; j < hi && ok; ++j) {
+                const uint32_t hj = h0 + (uint32_t)(j - lo);
+                const uint32_t nv = r0 + 2u * (uint32_t)(j - lo), nk = nv + 1;
+                if (!full(nv)) break;                                      // V_j
+                if (hj > 0 && !wait(&bars->dp_free, (hj - 1) & 1)) break;  // dP(j-1) read
+                tc_fence_after_sync();
+                mm_kk(C::DQ_DP_COL, fixB_k, slot(nv));                     // dP(j) = dO V_j^T
+                commit(&bars->ring_empty[slot(nv)]);
+                if (j == hi - 1) commit(&bars->fix_empty);                 // last use of Q, dO
+                if (j > lo) {
+                    // s_full(j) is committed only after p_full(j-1) is seen: the compute warps
+                    // cannot start step j before finishing j-1 anyway, and so p_full never
+                    // runs a phase ahead of this wait.  It precedes the accumulation, so it
+                    // tracks S(j) and dP(j) only.
+                    if (!wait(&bars->p_full[0], (hj - 1) & 1)) break;
+                    commit(&bars->s_full[0]);
+                    if (!acc_started && !wait(&bars->acc_empty, (uc & 1) ^ 1)) break;
+                    tc_fence_after_sync();
+                    mm_acc(((hj - 1) & 1) * C::BUF_COLS, slot(nk - 2), acc_started);   // dQ += dS(j-1) K_{j-1}
+                    acc_started = true;
+                    commit(&bars->ring_empty[slot(nk - 2)]);
+                } else {
+                    commit(&bars->s_full[0]);     // the previous step's p_full was seen at its unit's end
+                }
+                if (j + 1 < hi) {
+                    // S buffer (j+1) & 1 was last read by the accumulation just issued
+                    if (!full(nk + 2)) break;                              // K_{j+1}
+                    tc_fence_after_sync();
+                    mm_kk(((hj + 1) & 1) * C::BUF_COLS, fixA_k, slot(nk + 2));
+                }
+            }
+            if (!ok) break;
+            const uint32_t hl = h0 + (uint32_t)(hi - 1 - lo);              // the unit's last step
+            if (!wait(&bars->p_full[0], hl & 1)) break;
+            if (!acc_started && !wait(&bars->acc_empty, (uc & 1) ^ 1)) break;
+            tc_fence_after_sync();
+            mm_acc((hl & 1) * C::BUF_COLS, slot(r0 + 2u * (uint32_t)(hi - 1 - lo) + 1), acc_started);
+            commit(&bars->ring_empty[slot(r0 + 2u * (uint32_t)(hi - 1 - lo) + 1)]);
+            commit(&bars->acc_done);
+            rc = r0 + 2u * (uint32_t)(hi - lo);
+            hs = h0 + (uint32_t)(hi - lo);
+            ++uc;
+        }
+        if (!ok && lane == 0) bwd_timeout(p, bars);
+        commit(&bars->drain);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        __syncwarp();
+      } else {
+        // ---------------------------------------------------------------- MMA, dK/dV pass
         regs_decrease<C::REG_CONTROL>();
         constexpr uint32_t idesc_kk = idesc_f32acc(1, 0, 128, C::BC);  // bf16, both K-major, N = 64
         constexpr uint32_t idesc_acc = idesc_f32acc(1, 1, 128, D);     // B MN-major, N = D
@@ -316,7 +434,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             int bh, t;
             if (!bwd_unit(p, su, bh, t)) continue;
             int lo, hi;
-            bwd_steps(p, t, !kDQ, lo, hi);
+            bwd_steps(p, t, !kDQ, C::BC, lo, hi);
             if (!wait(&bars->fix_full, uc & 1)) break;
             tc_fence_after_sync();
             bool acc_started = false;
@@ -369,6 +487,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         commit(&bars->drain);
         mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
         __syncwarp();
+      }
     } else if (warp < C::COMPUTE_WARPS) {
         // ---------------------------------------------------------------- compute warpgroups
         // warpgroup wg takes the steps whose global index h has h & 1 == wg (TMEM buffer
@@ -389,8 +508,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
         };
         // dK/dV pass: lane l holds the LSE (log2 units) and D of columns c + 2l, c + 2l + 1
         // of a step; each warp keeps its own copy in shared memory while it works on it
-        float* my_lse2 = bars->col[warp][0];
-        float* my_delta = bars->col[warp][1];
+        float* my_lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512) + warp * 128;
+        float* my_delta = my_lse2 + 64;
         auto col_load = [&](int bh, int c, float2& l2v, float2& dv) {
             const size_t base = (size_t)bh * p.N;
             const int c0 = min(c + 2 * lane, p.N - 1), c1 = min(c + 2 * lane + 1, p.N - 1);
@@ -401,7 +520,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             int bh, t;
             if (!bwd_unit(p, su, bh, t)) continue;
             int lo, hi;
-            bwd_steps(p, t, !kDQ, lo, hi);
+            bwd_steps(p, t, !kDQ, C::BC, lo, hi);
             const int my = t * 128 + trow;              // this thread's row (query or key)
             const bool valid = my < p.N;
             float lse2 = 0.0f, dlt = 0.0f;              // dQ pass: per-row LSE and D
@@ -425,6 +544,67 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
             }
             m_hi = min(m_hi, p.N - 1);
             const uint32_t m_span = (uint32_t)(m_hi - m_lo);
+          if constexpr (kDQ) {
+            // dQ pass: both warpgroups work on every step, warpgroup wg on keys
+            // [64 wg, 64 wg + 64) of it; dP is released as soon as it is in registers
+            const uint32_t h0 = h;                      // global index of step lo
+            h = h0 + (uint32_t)(hi - lo);
+            for (int j = lo; j < hi; ++j) {
+                const uint32_t hj = h0 + (uint32_t)(j - lo);
+                const int c0 = j * C::BC + wg * 64;     // this warpgroup's first key
+                if (!wait_all(&bars->s_full[0], hj & 1)) break;
+                tc_fence_after_sync();
+                const uint32_t sb = tmem + lane_addr + (hj & 1) * C::BUF_COLS + (uint32_t)wg * 64;
+                const uint32_t db = tmem + lane_addr + C::DQ_DP_COL + (uint32_t)wg * 64;
+                uint32_t sra[64], dra[64];
+                tmem_ld32p(sb, sra);
+                tmem_ld32p(sb + 32, sra + 32);
+                tmem_ld32p(db, dra);
+                tmem_ld32p(db + 32, dra + 32);
+                tmem_wait_ld_only();
+                reg_fence32(sra);
+                reg_fence32(sra + 32);
+                reg_fence32(dra);
+                reg_fence32(dra + 32);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->dp_free));
+                // dS = P * (dP - D) of this thread's row over the warpgroup's 64 keys, packed to
+                // bf16 pairs over the first 32 of its S columns (already in registers)
+                auto stepq = [&](auto masked_tag) {
+                    constexpr bool kMasked = decltype(masked_tag)::value;
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float dsv[2];
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int i = ch * 32 + 2 * e + h2;
+                                float pr = ex2(fmaf(__uint_as_float(sra[i]), p.c_log2, -lse2));
+                                if constexpr (kMasked) {
+                                    // key c0 + i is allowed iff it lies in [m_lo, m_hi]
+                                    const uint32_t off = (uint32_t)(c0 - m_lo) + (uint32_t)i;
+                                    pr = off <= m_span ? pr : 0.0f;
+                                }
+                                dsv[h2] = pr * (__uint_as_float(dra[i]) - dlt);
+                            }
+                            pk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                        }
+                        tmem_st16p(sb + ch * 16, pk);
+                    }
+                };
+                if (bwd_block_full(p, t * 128, 128, j * C::BC, C::BC))
+                    stepq(std::false_type{});
+                else
+                    stepq(std::true_type{});
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[0]));
+            }
+          } else {
             const uint32_t h0 = h;                      // global index of step lo
             h = h0 + (uint32_t)(hi - lo);
             int s = lo + (int)((h0 ^ (uint32_t)wg) & 1u);   // this warpgroup's first step
@@ -518,6 +698,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[wg]));
             }
+          }
             if (!ok) break;
             // epilogue: dQ (or dV, dK) from TMEM, times scale where it applies, to bf16.
             // dQ pass: each warpgroup writes half of dQ's columns; dK/dV pass: warpgroup 0
@@ -567,7 +748,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::NUM_THREADS, 1)
 template <int D>
 cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cudaStream_t stream)
 {
-    using C = BwdCfg<D>;
+    using CQ = BwdCfg<D, true>;
+    using CKV = BwdCfg<D, false>;
     const long long rows = (long long)p.BH * p.N;
     bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
@@ -576,19 +758,20 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cud
     const int grid = pairs < sm_count ? pairs : sm_count;
     auto kq = bwd_kernel<D, true>;
     auto kkv = bwd_kernel<D, false>;
-    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES)) != cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, CKV::SMEM_BYTES)) != cudaSuccess)
         return e;
     // setmaxnreg.inc would wait forever if the launch pool were smaller than the split
     for (const void* f : {reinterpret_cast<const void*>(kq), reinterpret_cast<const void*>(kkv)}) {
         cudaFuncAttributes attr;
         if ((e = cudaFuncGetAttributes(&attr, f)) != cudaSuccess) return e;
-        if (attr.numRegs * C::NUM_THREADS < C::REG_POOL) return cudaErrorInvalidConfiguration;
+        if (attr.numRegs * CQ::NUM_THREADS < CQ::REG_POOL) return cudaErrorInvalidConfiguration;
     }
-    kq<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.q, m.dout, m.k64, m.v64, p);
+    // dQ pass: ring K and V with 128-row boxes; dK/dV pass: ring Q and dO with 64-row boxes
+    kq<<<grid, CQ::NUM_THREADS, CQ::SMEM_BYTES, stream>>>(m.q, m.dout, m.k, m.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kkv<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(m.k, m.v, m.q64, m.dout64, p);
+    kkv<<<grid, CKV::NUM_THREADS, CKV::SMEM_BYTES, stream>>>(m.k, m.v, m.q64, m.dout64, p);
     return cudaGetLastError();
 }
 
