@@ -54,9 +54,13 @@ struct BwdCfg {
     static constexpr int SMEM_CAP = 227 * 1024;
     static constexpr int BAR_BYTES = kDQ ? 512 : 512 + 4096;   // barriers (+ dK/dV: per-warp LSE / D)
     static constexpr int ALIGN_SLACK = 1024;
-    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * FIX_BYTES) / RING_BYTES;
+    // A ring slot holds one tile (dQ pass: V_j and K_j have different lifetimes) or a
+    // step's two tiles under one barrier pair (dK/dV pass: Q_i and dO_i are used alike).
+    static constexpr int TILES_PER_SLOT = kDQ ? 1 : 2;
+    static constexpr int SLOT_BYTES = TILES_PER_SLOT * RING_BYTES;
+    static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - 2 * FIX_BYTES) / SLOT_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
-    static constexpr int SMEM_BYTES = ALIGN_SLACK + 2 * FIX_BYTES + NSLOT * RING_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = ALIGN_SLACK + 2 * FIX_BYTES + NSLOT * SLOT_BYTES + BAR_BYTES;
     // TMEM.  dQ pass: S of step h in buffer h & 1 at 128 (h & 1) (then dS, packed), dP at
     // DQ_DP_COL, dQ at ACC_COL.  dK/dV pass: step buffer h & 1 at 128 (h & 1) holds S^T at
     // +S_OFF (then P^T) and dP^T at +DP_OFF (then dS^T); dV at ACC_COL, dK at ACC_COL + D.
@@ -77,7 +81,7 @@ struct BwdCfg {
     static constexpr int REG_POOL = 256 * REG_COMPUTE + 128 * REG_CONTROL;
     static_assert(D == 64 || D == 128, "backward head dim");
     static_assert(kDQ ? ACC_COL + D <= TMEM_COLS : ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
-    static_assert(NSLOT >= (kDQ ? 5 : 6), "ring too small");
+    static_assert(NSLOT >= (kDQ ? 5 : 4), "ring too small");
     static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
 };
 
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                                                ~uintptr_t(1023));
     uint8_t* fix = smem;                                   // 2 fixed tiles
     uint8_t* ring = smem + 2 * C::FIX_BYTES;               // NSLOT ring tiles
-    BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::RING_BYTES);
+    BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::SLOT_BYTES);
     const volatile int* abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsub = 2 * ((p.nt + 1) >> 1) * p.BH;   // sub-units (see bwd_unit)
@@ -259,21 +263,24 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 for (int s = lo; s < hi && ok; ++s) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
+                        // dQ pass: V_j then K_j, a slot each; dK/dV pass: Q_i then dO_i, one slot
                         const uint32_t slot = rc % C::NSLOT;
-                        if (!mbar_wait(smem_u32(&bars->ring_empty[slot]), ((rc / C::NSLOT) & 1) ^ 1,
-                                       abort_flag, p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
                         const uint32_t rb = smem_u32(&bars->ring_full[slot]);
-                        mbar_arrive_expect_tx(rb, C::RING_BYTES);
-                        // dQ pass: V_j then K_j; dK/dV pass: Q_i then dO_i
+                        if (kDQ || which == 0) {
+                            if (!mbar_wait(smem_u32(&bars->ring_empty[slot]), ((rc / C::NSLOT) & 1) ^ 1,
+                                           abort_flag, p.timeout_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(rb, C::SLOT_BYTES);
+                        }
                         const CUtensorMap* map = (which == 0) == kDQ ? &tmRingB : &tmRingA;
+                        uint8_t* dst = ring + slot * C::SLOT_BYTES + (kDQ ? 0 : which * C::RING_BYTES);
 #pragma unroll
                         for (int cb = 0; cb < C::NCB; ++cb)
-                            tma_load_3d(smem_u32(ring + slot * C::RING_BYTES + cb * C::RING_CB), map, rb,
-                                        cb * 64, s * C::BC, bh, pol_ring);
-                        ++rc;
+                            tma_load_3d(smem_u32(dst + cb * C::RING_CB), map, rb, cb * 64, s * C::BC, bh,
+                                        pol_ring);
+                        if (kDQ || which == 1) ++rc;
                     }
                 }
                 ++uc;
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         auto full = [&](uint32_t n) -> bool { return wait(&bars->ring_full[n % C::NSLOT], (n / C::NSLOT) & 1); };
         // D[128 x 128] = A[128 x D] (fixed tile) B[128 x D]^T (ring tile in slot sl), K = D
         auto mm_kk = [&](uint32_t d_col, uint64_t a0, uint32_t sl) {
-            const uint64_t b0 = ring_k + (uint64_t)((sl * C::RING_BYTES) >> 4);
+            const uint64_t b0 = ring_k + (uint64_t)((sl * C::SLOT_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int byte = kk * 32;
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         // dQ (+)= dS (TMEM: bf16 pairs of keys 0-63 at a + [0, 32), keys 64-127 at
         // a + [64, 96), one run per compute warpgroup) * K_j (slot sl as MN-major, K = 128)
         auto mm_acc = [&](uint32_t a_col, uint32_t sl, bool accumulate) {
-            const uint64_t b0 = ring_mn + (uint64_t)((sl * C::RING_BYTES) >> 4);
+            const uint64_t b0 = ring_mn + (uint64_t)((sl * C::SLOT_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < C::BC / 16; ++kk)
                 mma_ts_warp<false>(tmem + C::ACC_COL, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
@@ -440,12 +447,12 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             bool acc_started = false;
             // accumulation of step h (its P / dS are in TMEM once p_full fires), then the
             // step's two ring tiles are free
-            auto issue_acc = [&](uint32_t h, uint32_t sa, uint32_t sb) -> bool {
+            auto issue_acc = [&](uint32_t h, uint32_t sa) -> bool {
                 if (!wait(&bars->p_full[h & 1], (h >> 1) & 1)) return false;
                 if (!acc_started && !wait(&bars->acc_empty, (uc & 1) ^ 1)) return false;
                 tc_fence_after_sync();
-                const uint64_t ma = ring_mn + (uint64_t)((sa * C::RING_BYTES) >> 4);
-                const uint64_t mb = ring_mn + (uint64_t)((sb * C::RING_BYTES) >> 4);
+                const uint64_t ma = ring_mn + (uint64_t)((sa * C::SLOT_BYTES) >> 4);               // Q_i
+                const uint64_t mb = ring_mn + (uint64_t)((sa * C::SLOT_BYTES + C::RING_BYTES) >> 4);  // dO_i
                 const uint32_t bc = (h & 1) * C::BUF_COLS;
                 if constexpr (kDQ) {
                     mm_acc(C::ACC_COL, bc + C::S_OFF, ma, acc_started);          // dQ += dS K
@@ -455,31 +462,28 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 }
                 acc_started = true;
                 commit(&bars->ring_empty[sa]);
-                commit(&bars->ring_empty[sb]);
                 return true;
             };
-            uint32_t psa = 0, psb = 0;
+            uint32_t psa = 0;
             bool pend = false;
             for (int s = lo; s < hi; ++s) {
-                const uint32_t sa = rc % C::NSLOT, sb = (rc + 1) % C::NSLOT;
+                const uint32_t sa = rc % C::NSLOT;       // Q_i and dO_i of this step
                 if (!wait(&bars->ring_full[sa], (rc / C::NSLOT) & 1)) break;
-                if (!wait(&bars->ring_full[sb], ((rc + 1) / C::NSLOT) & 1)) break;
                 tc_fence_after_sync();
                 // buffer hs & 1 was last read by step hs - 2's accumulation, issued earlier
                 const uint32_t bc = (hs & 1) * C::BUF_COLS;
-                mm_kk(bc + C::S_OFF, fixA_k, ring_k + (uint64_t)((sa * C::RING_BYTES) >> 4));   // S (S^T)
-                mm_kk(bc + C::DP_OFF, fixB_k, ring_k + (uint64_t)((sb * C::RING_BYTES) >> 4));  // dP (dP^T)
+                mm_kk(bc + C::S_OFF, fixA_k, ring_k + (uint64_t)((sa * C::SLOT_BYTES) >> 4));                 // S^T
+                mm_kk(bc + C::DP_OFF, fixB_k, ring_k + (uint64_t)((sa * C::SLOT_BYTES + C::RING_BYTES) >> 4));  // dP^T
                 commit(&bars->s_full[hs & 1]);
                 if (s == hi - 1) commit(&bars->fix_empty);
-                if (pend && !issue_acc(hs - 1, psa, psb)) break;
+                if (pend && !issue_acc(hs - 1, psa)) break;
                 psa = sa;
-                psb = sb;
                 pend = true;
                 ++hs;
-                rc += 2;
+                rc += 1;
             }
             if (!ok) break;
-            if (!issue_acc(hs - 1, psa, psb)) break;
+            if (!issue_acc(hs - 1, psa)) break;
             commit(&bars->acc_done);
             ++uc;
         }
