@@ -20,7 +20,11 @@ Functions and the passage each follows:
   online_replay_f64          block-wise online softmax ([WGC] §2 GEMM-Softmax 融合流水线)
   key_allowed                mask sets ([YT] §2.1.2 稀疏性感知的Mask优化)
   e4m3_encode / e4m3_decode  E4M3 format ([JJ] §1.5 低精度FP8)
-  quantize_fp8_blockwise     per-block scaling ([WGC] §3 FP8 量化与精度保持)
+  e5m2_encode / e5m2_decode  E5M2 format, the wider-range one ([JJ] §1.5; [WGC] §3 lists
+                             both formats)
+  quantize_fp8_blockwise     per-block scaling ([WGC] §3 FP8 量化与精度保持), into E4M3
+                             (fmt="e4m3", scale = amax/448) or E5M2 (fmt="e5m2",
+                             scale = amax/57344)
   dequantize                 x ~= x8 * scale for the block, the inverse map
   hadamard_rotate_f32        incoherent processing before quantisation ([JJ] §1
                              item 3, 块量化和无相关处理): orthonormal Walsh-Hadamard
@@ -98,6 +102,14 @@ def _load():
         lib.oracle_e4m3_encode_array.restype = None
         lib.oracle_quantize_fp8_blockwise.argtypes = [fp, u8p, fp, L, L, L, L]
         lib.oracle_quantize_fp8_blockwise.restype = None
+        lib.oracle_e5m2_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e5m2_encode.restype = ctypes.c_uint8
+        lib.oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e5m2_decode.restype = ctypes.c_float
+        lib.oracle_e5m2_encode_array.argtypes = [fp, u8p, L]
+        lib.oracle_e5m2_encode_array.restype = None
+        lib.oracle_quantize_fp8_blockwise_fmt.argtypes = [fp, u8p, fp, L, L, L, L, I]
+        lib.oracle_quantize_fp8_blockwise_fmt.restype = None
         lib.oracle_hadamard_rotate_f32.argtypes = [fp, fp, L, L, ctypes.c_float]
         lib.oracle_hadamard_rotate_f32.restype = None
         _lib = lib
@@ -280,8 +292,28 @@ def e4m3_decode(codes) -> np.ndarray:
     return table[np.asarray(codes, dtype=np.uint8)]
 
 
-def quantize_fp8_blockwise(x, block: int = 128):
-    """x: [..., N, d] (bf16 values) -> (x8 uint8 [..., N, d], scales float32 [..., ceil(N/block)])."""
+def e5m2_encode(x) -> np.ndarray:
+    """float32 array -> uint8 E5M2 codes (RNE, saturating to +-57344)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e5m2_encode_array(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_uint8),
+                                     x.size)
+    return out
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """uint8 E5M2 codes -> float32 values (exact; exponent field 31 gives inf / NaN)."""
+    lib = _load()
+    table = np.array([lib.oracle_e5m2_decode(c) for c in range(256)], dtype=np.float32)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def quantize_fp8_blockwise(x, block: int = 128, fmt: str = "e4m3"):
+    """x: [..., N, d] (bf16 values) -> (x8 uint8 [..., N, d], scales float32 [..., ceil(N/block)]).
+    fmt "e4m3" (scale = amax/448) or "e5m2" (scale = amax/57344)."""
     if hasattr(x, "detach"):
         import torch
         x = x.detach().to("cpu").to(torch.float32).numpy()
@@ -292,8 +324,13 @@ def quantize_fp8_blockwise(x, block: int = 128):
     nblk = (N + block - 1) // block
     x8 = np.empty(shape, dtype=np.uint8)
     scales = np.empty(shape[:-2] + (nblk,), dtype=np.float32)
-    _load().oracle_quantize_fp8_blockwise(_ptr(x, ctypes.c_float), _ptr(x8, ctypes.c_uint8),
-                                          _ptr(scales, ctypes.c_float), BH, N, d, int(block))
+    if fmt == "e4m3":
+        _load().oracle_quantize_fp8_blockwise(_ptr(x, ctypes.c_float), _ptr(x8, ctypes.c_uint8),
+                                              _ptr(scales, ctypes.c_float), BH, N, d, int(block))
+    else:
+        _load().oracle_quantize_fp8_blockwise_fmt(_ptr(x, ctypes.c_float), _ptr(x8, ctypes.c_uint8),
+                                                  _ptr(scales, ctypes.c_float), BH, N, d, int(block),
+                                                  FP8_FORMATS[fmt])
     return x8, scales
 
 
@@ -325,11 +362,11 @@ def quantize_fp8_hadamard(x, block: int = 128):
     return quantize_fp8_blockwise(hadamard_rotate_f32(x), block)
 
 
-def dequantize(x8, scales, block: int = 128) -> np.ndarray:
+def dequantize(x8, scales, block: int = 128, fmt: str = "e4m3") -> np.ndarray:
     """x_hat = decode(x8) * scale of its row block, in float64 (exact products)."""
     x8 = np.asarray(x8, dtype=np.uint8)
     scales = np.asarray(scales, dtype=np.float32)
-    vals = e4m3_decode(x8).astype(np.float64)
+    vals = (e4m3_decode(x8) if fmt == "e4m3" else e5m2_decode(x8)).astype(np.float64)
     N = x8.shape[-2]
     row_scale = np.repeat(scales.astype(np.float64), block, axis=-1)[..., :N]
     return vals * row_scale[..., None]

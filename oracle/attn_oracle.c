@@ -304,6 +304,85 @@ void oracle_quantize_fp8_blockwise(const float* x, uint8_t* x8, float* scales, l
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* FP8 E5M2 codec, written from the OCP 8-bit floating point definition:      */
+/*   1 sign bit, 5 exponent bits with bias 15, 2 mantissa bits;               */
+/*   exponent field 0 holds subnormals m * 2^-16; exponent field 31 holds     */
+/*   infinity (mantissa 0) and NaN (mantissa != 0); largest finite 57344.     */
+/* [JJ] §1.5 低精度FP8 names E5M2 as the 5-exponent / 2-mantissa format with   */
+/* the wider range; [WGC] §3 lists both formats.  Encoding rounds to nearest, */
+/* ties to even, and saturates out-of-range magnitudes (and infinities) to    */
+/* +-57344 ("satfinite"), as the E4M3 encoder does to +-448.                  */
+/* ------------------------------------------------------------------------- */
+uint8_t oracle_e5m2_encode(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    if (isinf(x)) return (uint8_t)(sign | 0x7B);
+    const double a = fabs((double)x);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: units of 2^-16; the integer 4 is the smallest normal (code 0x04) */
+        const double units = rint(a * 65536.0); /* exact scaling, ties to even */
+        return (uint8_t)(sign | (uint8_t)units);
+    }
+    int e2;
+    (void)frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1) */
+    int e = e2 - 1;      /* a in [2^e, 2^(e+1)) */
+    double r = rint(ldexp(a, 2 - e)); /* mantissa with 2 fraction bits, in [4, 8] */
+    if (r == 8.0) { r = 4.0; e += 1; }
+    if (e > 15) return (uint8_t)(sign | 0x7B);
+    const int code = ((e + 15) << 2) | ((int)r - 4);
+    if (code > 0x7B) return (uint8_t)(sign | 0x7B);
+    return (uint8_t)(sign | code);
+}
+
+float oracle_e5m2_decode(uint8_t c)
+{
+    const double sgn = (c & 0x80) ? -1.0 : 1.0;
+    const int e = (c >> 2) & 0x1F, m = c & 0x3;
+    if (e == 0x1F) return (m == 0) ? (float)(sgn * INFINITY) : NAN;
+    if (e == 0) return (float)(sgn * ldexp((double)m, -16));
+    return (float)(sgn * ldexp(1.0 + m / 4.0, e - 15));
+}
+
+void oracle_e5m2_encode_array(const float* x, uint8_t* out, long n)
+{
+#pragma omp parallel for schedule(static)
+    for (long t = 0; t < n; ++t) out[t] = oracle_e5m2_encode(x[t]);
+}
+
+/*
+ * Per-block FP8 quantisation into either format: as oracle_quantize_fp8_blockwise,
+ * with the format's largest finite value in place of 448:
+ *   fmt 0 (E4M3): scale = amax / 448,   x8 = e4m3(x / scale)
+ *   fmt 1 (E5M2): scale = amax / 57344, x8 = e5m2(x / scale)
+ */
+void oracle_quantize_fp8_blockwise_fmt(const float* x, uint8_t* x8, float* scales, long BH, long N,
+                                       long d, long block, int fmt)
+{
+    const long nblk = (N + block - 1) / block;
+    const float fmax = fmt ? 57344.0f : 448.0f;
+#pragma omp parallel for schedule(static)
+    for (long u = 0; u < BH * nblk; ++u) {
+        const long h = u / nblk, b = u % nblk;
+        const long r0 = b * block, r1 = (r0 + block < N) ? r0 + block : N;
+        const float* xb = x + (h * N + r0) * d;
+        uint8_t* yb = x8 + (h * N + r0) * d;
+        const long cnt = (r1 - r0) * d;
+        float amax = 0.0f;
+        for (long t = 0; t < cnt; ++t) {
+            const float a = fabsf(xb[t]);
+            if (a > amax) amax = a;
+        }
+        const float scale = (amax > 0.0f) ? amax / fmax : 1.0f;
+        for (long t = 0; t < cnt; ++t) {
+            const float qv = xb[t] / scale;
+            yb[t] = fmt ? oracle_e5m2_encode(qv) : oracle_e4m3_encode(qv);
+        }
+        scales[u] = scale;
+    }
+}
+
 /*
  * Incoherent processing before FP8 quantisation ("大模型加速-核心网络算子-Flash
  * Attention V3", §1 item 3 and the closing summary: block quantisation together
