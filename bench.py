@@ -433,6 +433,17 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
         out["fp8_causal" if causal else "fp8"] = {
             "tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
             "peak": peak8, "peak_source": "fp8 = 2 x measured bf16 burst (nominal ratio)"}
+    # mixed FP8 formats: Q and K quantised to E5M2 (amax / 57344), V kept in E4M3
+    qe, sqe = fa.attn_quantize_fp8_blockwise_fmt(q2d, "e5m2")
+    ke, ske = fa.attn_quantize_fp8_blockwise_fmt(k2d, "e5m2")
+
+    def fp8_e5m2_step():
+        fa.attn_fwd_fp8_fmt(qe, ke, v8, sqe, ske, sv, "e5m2", scale=scale, o=o, lse=lse, stream=stream)
+    ms, per = time_steps(fp8_e5m2_step, reps, 3, stream)
+    t = flops(B, H, N, D) / (statistics.mean(per) * 1e-3) / 1e12
+    out["fp8_qk_e5m2"] = {"tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
+                          "formats": "Q, K E5M2; V, P E4M3"}
+    del qe, ke, sqe, ske
     # packed variable-length sequences: the same 131072 tokens as lengths uniform in
     # [512, 16384] (seeded), non-causal and causal; FLOPs over the allowed pairs
     from exact_attention_55_gb300.inputs import make_packed_qkv, varlen_lengths

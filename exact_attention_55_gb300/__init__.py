@@ -31,6 +31,7 @@ __all__ = [
     "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_bf16_paged_noalloc",
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
+    "attn_quantize_fp8_blockwise_fmt", "attn_fwd_fp8_fmt", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
 ]
@@ -42,13 +43,18 @@ ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 
+ATTN_FP8_E4M3 = 0
+ATTN_FP8_E5M2 = 1
+_FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2,
+                ATTN_FP8_E4M3: ATTN_FP8_E4M3, ATTN_FP8_E5M2: ATTN_FP8_E5M2}
+
 EXPORTED_SYMBOLS = (
     "attn_fwd_bf16", "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_fwd_bf16_varlen",
     "attn_decode_bf16_paged",
     "attn_decode_bf16_paged_noalloc", "attn_decode_workspace_bytes",
-    "attn_quantize_fp8_blockwise",
+    "attn_quantize_fp8_blockwise", "attn_quantize_fp8_blockwise_fmt",
     "attn_quantize_fp8_hadamard",
-    "attn_fwd_fp8", "attn_status_string", "attn_get_device_status",
+    "attn_fwd_fp8", "attn_fwd_fp8_fmt", "attn_status_string", "attn_get_device_status",
     "attn_selftest_wait_timeout",
 )
 
@@ -101,6 +107,10 @@ def load_library(path: str | None = None):
         lib.attn_quantize_fp8_hadamard.restype = i
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.attn_fwd_fp8.restype = i
+        lib.attn_quantize_fp8_blockwise_fmt.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.attn_quantize_fp8_blockwise_fmt.restype = i
+        lib.attn_fwd_fp8_fmt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+        lib.attn_fwd_fp8_fmt.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -335,6 +345,25 @@ def attn_quantize_fp8_blockwise(x, block: int = 128, x8=None, scales=None, strea
     return x8, scales
 
 
+def _fp8_format(fmt) -> int:
+    if fmt not in _FP8_FORMATS:
+        raise ValueError(f"unknown FP8 format {fmt!r} (use 'e4m3' or 'e5m2')")
+    return _FP8_FORMATS[fmt]
+
+
+def attn_quantize_fp8_blockwise_fmt(x, fmt, block: int = 128, x8=None, scales=None, stream=None):
+    """Per-(head, 128-row block) quantisation into E4M3 ('e4m3': scale = amax/448) or
+    E5M2 ('e5m2': scale = amax/57344); returns (x8 uint8 codes, fp32 scales)."""
+    _check_bhnd("x", x, torch.bfloat16)
+    B, H, N, d = x.shape
+    x8, scales = _quant_outputs(x, block, x8, scales)
+    st = load_library().attn_quantize_fp8_blockwise_fmt(x.data_ptr(), x8.data_ptr(),
+                                                        scales.data_ptr(), B, H, N, d, int(block),
+                                                        _fp8_format(fmt), _stream_handle(stream))
+    _raise_if(st, "attn_quantize_fp8_blockwise_fmt")
+    return x8, scales
+
+
 def attn_quantize_fp8_hadamard(x, block: int = 128, x8=None, scales=None, stream=None):
     """Rows of x times the orthonormal Walsh-Hadamard matrix, then per-block E4M3
     quantisation (for Q and K); returns (x8 uint8 codes, fp32 scales)."""
@@ -351,10 +380,27 @@ def attn_quantize_fp8_hadamard(x, block: int = 128, x8=None, scales=None, stream
 def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | None = None,
                  causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
     """Forward pass on E4M3 operands (uint8 codes or float8_e4m3fn) with per-block descales."""
+    return _fwd_fp8("attn_fwd_fp8", None, q8, k8, v8, descale_q, descale_k, descale_v, scale,
+                    causal, window, o, lse, stream)
+
+
+def attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, qk_fmt, scale: float | None = None,
+                     causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
+    """attn_fwd_fp8 with Q and K both in qk_fmt ('e4m3' or 'e5m2', from
+    attn_quantize_fp8_blockwise_fmt); V stays E4M3."""
+    return _fwd_fp8("attn_fwd_fp8_fmt", _fp8_format(qk_fmt), q8, k8, v8, descale_q, descale_k,
+                    descale_v, scale, causal, window, o, lse, stream)
+
+
+def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, causal, window,
+             o, lse, stream):
+    views = []
     for n, t in (("q8", q8), ("k8", k8), ("v8", v8)):
-        if t.dtype == torch.float8_e4m3fn:
+        if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
             t = t.view(torch.uint8)
         _check_bhnd(n, t, torch.uint8)
+        views.append(t)
+    q8, k8, v8 = views
     if k8.shape != q8.shape or v8.shape != q8.shape:
         raise ValueError("q8, k8, v8 must have the same shape")
     B, H, N, d = q8.shape
@@ -368,12 +414,13 @@ def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | Non
     _check_out(lse, (B, H, N), torch.float32, q8.device, "lse")
     for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
         _check_out(t, (B, H, (N + 127) // 128), torch.float32, q8.device, n)
-    st = load_library().attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(),
-                                     descale_q.data_ptr(), descale_k.data_ptr(),
-                                     descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N,
-                                     d, float(scale), int(bool(causal)), int(window),
-                                     _stream_handle(stream))
-    _raise_if(st, "attn_fwd_fp8")
+    args = [q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), descale_q.data_ptr(), descale_k.data_ptr(),
+            descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
+            int(bool(causal)), int(window)]
+    if qk_fmt is not None:
+        args.append(qk_fmt)
+    st = getattr(load_library(), entry)(*args, _stream_handle(stream))
+    _raise_if(st, entry)
     return o, lse
 
 

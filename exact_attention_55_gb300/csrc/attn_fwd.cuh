@@ -317,7 +317,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
         // the tensor core.
         if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
         constexpr uint32_t fmt = F8 ? 0u : 1u;
-        constexpr uint32_t idesc_s = idesc_f32acc(fmt, 0, C::BM, C::BN);
+        // fp8: Q and K may both be E5M2 (format 1 of kind::f8f6f4); V and P stay E4M3, so
+        // each MMA's two operands always share one type
+        const uint32_t idesc_s = F8 ? idesc_f32acc(p.qk_fmt ? 1u : 0u, 0, C::BM, C::BN)
+                                    : idesc_f32acc(fmt, 0, C::BM, C::BN);
         constexpr uint32_t idesc_o = idesc_f32acc(fmt, 1, C::BM, D);
         const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem), 16, 1024);
         const uint64_t k_desc0 = sdesc_sw128(smem_u32(kv_smem), 16, 1024);

@@ -28,6 +28,7 @@ struct FwdParams {
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
     unsigned long long timeout_ns;  // bound on every mbarrier wait
+    int qk_fmt;           // fp8 path: format of the Q and K codes, 0 E4M3, 1 E5M2 (V is E4M3)
     // Packed variable-length sequences (null cu_seqlens: the batched [BH, N, D] layout).
     // q, k, v, o are [T, H, D]; lse is [H, T]; sequence s is tokens [cu[s], cu[s+1]).
     // Units are (sequence, head, pair of query blocks) with num_qblk from max_seqlen.
@@ -81,12 +82,13 @@ struct DecodeParams {
 
 struct QuantParams {
     const void* x;        // bf16 [BH, N, d]
-    uint8_t* x8;          // e4m3 [BH, N, d]
+    uint8_t* x8;          // e4m3 or e5m2 codes [BH, N, d]
     float* scales;        // fp32 [BH, ceil(N/128)]
     int* status;          // device status word (timeouts)
     int BH, N, d;
     int nblk;             // ceil(N / 128)
     int rotate;           // 1: Walsh-Hadamard rotation of each row before quantising
+    int fmt;              // 0: E4M3 codes, scale = amax / 448; 1: E5M2, scale = amax / 57344
     float rot_c;          // rotation normalisation fp32(1 / sqrt(d))
 };
 

@@ -412,6 +412,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // Pack two floats into e4m3x2 (round to nearest even, saturate to +-448): `lo` in bits 0-7.
+__device__ __forceinline__ uint16_t pack_e5m2x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
 {
     uint16_t r;

@@ -1,4 +1,4 @@
-// quant_fp8.cu -- per-block FP8-E4M3 quantisation of a bf16 [BH, N, d] tensor.
+// quant_fp8.cu -- per-block FP8 quantisation (E4M3, or E5M2) of a bf16 [BH, N, d] tensor.
 //
 // "Warp Group Cluster 优化：Flash Attention V3 在 H100 上的 FP8 融合计算实践",
 // §3 FP8 量化与精度保持: a scale factor computed per block maps the block's range
@@ -8,6 +8,9 @@
 // For each (head, block of 128 rows, all d columns):
 //   amax  = max |x|;  scale = amax / 448 (IEEE fp32 division), or 1 when amax == 0
 //   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 quotient, one rounding to E4M3)
+// The E5M2 variant (the pages' wider-range format, "大模型加速-核心网络算子-Flash
+// Attention V3" §1.5) divides amax by 57344, its largest finite value, and rounds
+// the same quotient to E5M2.
 //
 // HBM-bound design: persistent CTAs, as many per SM as fit (two at d = 128),
 // each stream whole blocks (one contiguous run of rows * d * 2 bytes) into a
@@ -104,7 +107,8 @@ template <int DR> struct QuantShape {
 };
 
 // DR = 0: plain per-block quantisation (any d); DR = d in {64, 128, 256}: rotate first.
-template <int DR>
+// FMT = 0: E4M3; FMT = 1: E5M2 (plain quantisation only).
+template <int DR, int FMT = 0>
 __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMinBlocks)
     quant_fp8_kernel(const QuantParams p)
 {
@@ -178,8 +182,11 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
             }
             amax = block_amax(amax);
-            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            scale = (amax > 0.0f) ? __fdiv_rn(amax, FMT ? 57344.0f : 448.0f) : 1.0f;
             const float y = __frcp_rn(scale);
+            auto pack2 = [](float lo, float hi) -> uint32_t {
+                return FMT ? pack_e5m2x2(lo, hi) : pack_e4m3x2(lo, hi);
+            };
 
             uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
             for (int g = threadIdx.x; g < nchunk; g += kThreads) {
@@ -188,10 +195,10 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 uint32_t out[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const uint32_t lo = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
-                                                    div_by_scale(bf16_hi(w[2 * e]), scale, y));
-                    const uint32_t hi = pack_e4m3x2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
-                                                    div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
+                    const uint32_t lo = pack2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
+                                              div_by_scale(bf16_hi(w[2 * e]), scale, y));
+                    const uint32_t hi = pack2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
+                                              div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
                     out[e] = lo | (hi << 16);
                 }
                 __stcs(dst + g, make_uint2(out[0], out[1]));
@@ -308,12 +315,12 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
     }
 }
 
-template <int DR>
+template <int DR, int FMT = 0>
 static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
     const int total = p.BH * p.nblk;
     const int smem = quant_smem_bytes(p.d);
-    auto kernel = quant_fp8_kernel<DR>;
+    auto kernel = quant_fp8_kernel<DR, FMT>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 1;  // CTAs that fit on one SM (two at d = 128, four at d = 64)
@@ -329,7 +336,8 @@ static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
-    if (!p.rotate) return launch_quant<0>(p, sm_count, stream);
+    if (!p.rotate) return p.fmt ? launch_quant<0, 1>(p, sm_count, stream) : launch_quant<0, 0>(p, sm_count, stream);
+    if (p.fmt) return cudaErrorInvalidValue;    // the rotated variant writes E4M3 only
     switch (p.d) {
     case 64: return launch_quant<64>(p, sm_count, stream);
     case 128: return launch_quant<128>(p, sm_count, stream);
