@@ -23,8 +23,9 @@ Functions and the passage each follows:
   e5m2_encode / e5m2_decode  E5M2 format, the wider-range one ([JJ] §1.5; [WGC] §3 lists
                              both formats)
   quantize_fp8_blockwise     per-block scaling ([WGC] §3 FP8 量化与精度保持), into E4M3
-                             (fmt="e4m3", scale = amax/448) or E5M2 (fmt="e5m2",
-                             scale = amax/57344)
+                             (fmt="e4m3", scale = amax/448), E5M2 (fmt="e5m2",
+                             scale = amax/57344), or E4M3 with a power-of-two scale per
+                             block (fmt="e4m3_pow2": the smallest 2^k >= amax/448)
   dequantize                 x ~= x8 * scale for the block, the inverse map
   hadamard_rotate_f32        incoherent processing before quantisation ([JJ] §1
                              item 3, 块量化和无相关处理): orthonormal Walsh-Hadamard
@@ -308,12 +309,13 @@ def e5m2_decode(codes) -> np.ndarray:
     return table[np.asarray(codes, dtype=np.uint8)]
 
 
-FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1, "e4m3_pow2": 2}
 
 
 def quantize_fp8_blockwise(x, block: int = 128, fmt: str = "e4m3"):
     """x: [..., N, d] (bf16 values) -> (x8 uint8 [..., N, d], scales float32 [..., ceil(N/block)]).
-    fmt "e4m3" (scale = amax/448) or "e5m2" (scale = amax/57344)."""
+    fmt "e4m3" (scale = amax/448), "e5m2" (scale = amax/57344) or "e4m3_pow2" (E4M3 codes,
+    scale = the smallest power of two >= amax/448)."""
     if hasattr(x, "detach"):
         import torch
         x = x.detach().to("cpu").to(torch.float32).numpy()
@@ -366,7 +368,7 @@ def dequantize(x8, scales, block: int = 128, fmt: str = "e4m3") -> np.ndarray:
     """x_hat = decode(x8) * scale of its row block, in float64 (exact products)."""
     x8 = np.asarray(x8, dtype=np.uint8)
     scales = np.asarray(scales, dtype=np.float32)
-    vals = (e4m3_decode(x8) if fmt == "e4m3" else e5m2_decode(x8)).astype(np.float64)
+    vals = (e5m2_decode(x8) if fmt == "e5m2" else e4m3_decode(x8)).astype(np.float64)
     N = x8.shape[-2]
     row_scale = np.repeat(scales.astype(np.float64), block, axis=-1)[..., :N]
     return vals * row_scale[..., None]

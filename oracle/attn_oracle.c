@@ -356,12 +356,23 @@ void oracle_e5m2_encode_array(const float* x, uint8_t* out, long n)
  * with the format's largest finite value in place of 448:
  *   fmt 0 (E4M3): scale = amax / 448,   x8 = e4m3(x / scale)
  *   fmt 1 (E5M2): scale = amax / 57344, x8 = e5m2(x / scale)
+ *   fmt 2 (E4M3 with power-of-two scales): s0 = amax / 448 (fp32), scale = the smallest
+ *          power of two >= s0 (a shared exponent per block, as in the OCP microscaling
+ *          formats; [WGC] §3 asks only for a per-block scale), x8 = e4m3(x / scale),
+ *          the quotient exact.
  */
+static float pow2_at_least(float s0)
+{
+    int e;
+    const float f = frexpf(s0, &e); /* s0 = f * 2^e, f in [0.5, 1) */
+    return (f == 0.5f) ? s0 : ldexpf(1.0f, e);
+}
+
 void oracle_quantize_fp8_blockwise_fmt(const float* x, uint8_t* x8, float* scales, long BH, long N,
                                        long d, long block, int fmt)
 {
     const long nblk = (N + block - 1) / block;
-    const float fmax = fmt ? 57344.0f : 448.0f;
+    const float fmax = (fmt == 1) ? 57344.0f : 448.0f;
 #pragma omp parallel for schedule(static)
     for (long u = 0; u < BH * nblk; ++u) {
         const long h = u / nblk, b = u % nblk;
@@ -374,10 +385,11 @@ void oracle_quantize_fp8_blockwise_fmt(const float* x, uint8_t* x8, float* scale
             const float a = fabsf(xb[t]);
             if (a > amax) amax = a;
         }
-        const float scale = (amax > 0.0f) ? amax / fmax : 1.0f;
+        float scale = (amax > 0.0f) ? amax / fmax : 1.0f;
+        if (fmt == 2 && amax > 0.0f) scale = pow2_at_least(scale);
         for (long t = 0; t < cnt; ++t) {
             const float qv = xb[t] / scale;
-            yb[t] = fmt ? oracle_e5m2_encode(qv) : oracle_e4m3_encode(qv);
+            yb[t] = (fmt == 1) ? oracle_e5m2_encode(qv) : oracle_e4m3_encode(qv);
         }
         scales[u] = scale;
     }

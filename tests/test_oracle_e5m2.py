@@ -114,3 +114,28 @@ def test_zero_block_and_e4m3_default_unchanged():
     b8, bsc = oracle.quantize_fp8_blockwise(q, 128, fmt="e4m3")
     np.testing.assert_array_equal(a8, b8)
     np.testing.assert_array_equal(asc, bsc)
+
+
+def test_power_of_two_scales():
+    """fmt e4m3_pow2: each block's scale is the smallest power of two at or above
+    fp32(amax / 448), and the codes are E4M3 of the exact quotient x / scale."""
+    q, _, _ = make_qkv(2, 3, 300, 128, seed=11, outliers=True)
+    x8, sc = oracle.quantize_fp8_blockwise(q, 128, fmt="e4m3_pow2")
+    _, sc448 = oracle.quantize_fp8_blockwise(q, 128)             # fp32(amax / 448)
+    m, e = np.frexp(sc)
+    assert (m == 0.5).all()                                      # powers of two
+    assert (sc >= sc448).all() and (sc < 2 * sc448).all()
+    xf = q.float().numpy()
+    rows = np.repeat(sc, 128, axis=-1)[..., :300]
+    quot = xf / rows[..., None]                                  # exact: power-of-two divisor
+    ref = torch.from_numpy(quot.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(x8, ref)
+    # the amax element lands in the top binade of E4M3: amax / scale is in (224, 448], which
+    # rounds to a code value of at least 224
+    dec = np.abs(oracle.e4m3_decode(x8).reshape(2, 3, 300, 128))
+    for b in range(3):
+        assert dec[:, :, 128 * b:128 * (b + 1)].max(axis=(-1, -2)).min() >= 224.0
+    # dequantised values are within half an E4M3 step of the input (relative 2^-4)
+    deq = oracle.dequantize(x8, sc, 128, fmt="e4m3_pow2")
+    normal = np.abs(xf) >= 2.0 ** -6 * rows[..., None]
+    assert (np.abs(deq - xf) / np.maximum(np.abs(xf), 1e-30))[normal].max() <= 2.0 ** -4
