@@ -32,6 +32,7 @@ __all__ = [
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
     "attn_quantize_fp8_blockwise_fmt", "attn_fwd_fp8_fmt", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
+    "ATTN_FP8_E4M3_POW2",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "EXPORTED_SYMBOLS",
 ]
@@ -45,8 +46,10 @@ ATTN_ERR_TIMEOUT = 5
 
 ATTN_FP8_E4M3 = 0
 ATTN_FP8_E5M2 = 1
-_FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2,
-                ATTN_FP8_E4M3: ATTN_FP8_E4M3, ATTN_FP8_E5M2: ATTN_FP8_E5M2}
+ATTN_FP8_E4M3_POW2 = 2   # E4M3 codes, power-of-two block scales
+_FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2, "e4m3_pow2": ATTN_FP8_E4M3_POW2,
+                ATTN_FP8_E4M3: ATTN_FP8_E4M3, ATTN_FP8_E5M2: ATTN_FP8_E5M2,
+                ATTN_FP8_E4M3_POW2: ATTN_FP8_E4M3_POW2}
 
 EXPORTED_SYMBOLS = (
     "attn_fwd_bf16", "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_fwd_bf16_varlen",
@@ -109,7 +112,7 @@ def load_library(path: str | None = None):
         lib.attn_fwd_fp8.restype = i
         lib.attn_quantize_fp8_blockwise_fmt.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
         lib.attn_quantize_fp8_blockwise_fmt.restype = i
-        lib.attn_fwd_fp8_fmt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+        lib.attn_fwd_fp8_fmt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, i, vp]
         lib.attn_fwd_fp8_fmt.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -347,13 +350,14 @@ def attn_quantize_fp8_blockwise(x, block: int = 128, x8=None, scales=None, strea
 
 def _fp8_format(fmt) -> int:
     if fmt not in _FP8_FORMATS:
-        raise ValueError(f"unknown FP8 format {fmt!r} (use 'e4m3' or 'e5m2')")
+        raise ValueError(f"unknown FP8 format {fmt!r} (use 'e4m3', 'e5m2' or 'e4m3_pow2')")
     return _FP8_FORMATS[fmt]
 
 
 def attn_quantize_fp8_blockwise_fmt(x, fmt, block: int = 128, x8=None, scales=None, stream=None):
-    """Per-(head, 128-row block) quantisation into E4M3 ('e4m3': scale = amax/448) or
-    E5M2 ('e5m2': scale = amax/57344); returns (x8 uint8 codes, fp32 scales)."""
+    """Per-(head, 128-row block) quantisation into E4M3 ('e4m3': scale = amax/448), E5M2
+    ('e5m2': scale = amax/57344) or E4M3 with power-of-two scales ('e4m3_pow2': the smallest
+    2^k >= amax/448); returns (x8 uint8 codes, fp32 scales)."""
     _check_bhnd("x", x, torch.bfloat16)
     B, H, N, d = x.shape
     x8, scales = _quant_outputs(x, block, x8, scales)
@@ -384,12 +388,14 @@ def attn_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, scale: float | Non
                     causal, window, o, lse, stream)
 
 
-def attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, qk_fmt, scale: float | None = None,
-                     causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
-    """attn_fwd_fp8 with Q and K both in qk_fmt ('e4m3' or 'e5m2', from
-    attn_quantize_fp8_blockwise_fmt); V stays E4M3."""
-    return _fwd_fp8("attn_fwd_fp8_fmt", _fp8_format(qk_fmt), q8, k8, v8, descale_q, descale_k,
-                    descale_v, scale, causal, window, o, lse, stream)
+def attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, qk_fmt, v_fmt="e4m3",
+                     scale: float | None = None, causal: bool = False, window: int = 0, o=None,
+                     lse=None, stream=None):
+    """attn_fwd_fp8 with Q and K both in qk_fmt ('e4m3', 'e5m2' or 'e4m3_pow2', from
+    attn_quantize_fp8_blockwise_fmt) and V in v_fmt ('e4m3' or 'e4m3_pow2': power-of-two
+    block scales, applied through P's exponent)."""
+    return _fwd_fp8("attn_fwd_fp8_fmt", (_fp8_format(qk_fmt), _fp8_format(v_fmt)), q8, k8, v8,
+                    descale_q, descale_k, descale_v, scale, causal, window, o, lse, stream)
 
 
 def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, causal, window,
@@ -418,7 +424,7 @@ def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, 
             descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
             int(bool(causal)), int(window)]
     if qk_fmt is not None:
-        args.append(qk_fmt)
+        args.extend(qk_fmt)
     st = getattr(load_library(), entry)(*args, _stream_handle(stream))
     _raise_if(st, entry)
     return o, lse

@@ -167,7 +167,7 @@ attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* 
 template <int D, bool F8>
 attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                       const float* dq, const float* dk, const float* dv, int BH, int N, float scale,
-                      int causal, int window, cudaStream_t stream, int qk_fmt = 0)
+                      int causal, int window, cudaStream_t stream, int qk_fmt = 0, int v_pow2 = 0)
 {
     using C = FwdCfg<D, F8>;
     DeviceInfo* dev = nullptr;
@@ -199,6 +199,7 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.c_log2 = (float)((double)scale * 1.4426950408889634);
     p.timeout_ns = kWaitTimeoutNs;
     p.qk_fmt = qk_fmt;
+    p.v_pow2 = v_pow2;
     if (launch_attn_fwd<D, F8>(mq, mk, mv, p, dev->sm_count, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -298,18 +299,22 @@ extern "C" attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void
                                       void* stream)
 {
     return attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale,
-                            causal, window, ATTN_FP8_E4M3, stream);
+                            causal, window, ATTN_FP8_E4M3, ATTN_FP8_E4M3, stream);
 }
 
 extern "C" attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const void* v8,
                                           const float* descale_q, const float* descale_k,
                                           const float* descale_v, void* o, float* lse, int B, int H,
                                           int N, int d, float scale, int causal, int window,
-                                          int qk_format, void* stream)
+                                          int qk_format, int v_format, void* stream)
 {
     if (!q8 || !k8 || !v8 || !descale_q || !descale_k || !descale_v || !o || !lse)
         return ATTN_ERR_INVALID_ARG;
-    if (qk_format != ATTN_FP8_E4M3 && qk_format != ATTN_FP8_E5M2) return ATTN_ERR_INVALID_ARG;
+    if (qk_format != ATTN_FP8_E4M3 && qk_format != ATTN_FP8_E5M2 && qk_format != ATTN_FP8_E4M3_POW2)
+        return ATTN_ERR_INVALID_ARG;
+    if (v_format != ATTN_FP8_E4M3 && v_format != ATTN_FP8_E4M3_POW2) return ATTN_ERR_INVALID_ARG;
+    const int qk_fmt = qk_format == ATTN_FP8_E5M2 ? 1 : 0;   // the codes' type in the QK^T MMA
+    const int v_pow2 = v_format == ATTN_FP8_E4M3_POW2 ? 1 : 0;
     long long BH = 0;
     attn_status_t st = check_common(B, H, N, scale, &BH);
     if (st != ATTN_OK) return st;
@@ -320,15 +325,17 @@ extern "C" attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const 
         return ATTN_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d == 128)
-        return run_fwd<128, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_format);
-    return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_format);
+        return run_fwd<128, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2);
+    return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2);
 }
 
 static attn_status_t quantize(const void* x, void* x8, float* scales, int B, int H, int N, int d,
                               int block, bool rotate, void* stream, int fmt = ATTN_FP8_E4M3)
 {
     if (!x || !x8 || !scales) return ATTN_ERR_INVALID_ARG;
-    if (fmt != ATTN_FP8_E4M3 && fmt != ATTN_FP8_E5M2) return ATTN_ERR_INVALID_ARG;
+    if (fmt != ATTN_FP8_E4M3 && fmt != ATTN_FP8_E5M2 && fmt != ATTN_FP8_E4M3_POW2)
+        return ATTN_ERR_INVALID_ARG;
+    if (rotate && fmt != ATTN_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
     if (block != 128 || d % 16 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
     if (rotate && d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;

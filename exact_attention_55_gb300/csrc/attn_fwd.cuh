@@ -494,7 +494,11 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 if (!p.causal) jhi = min(jhi, row + p.window);
             }
             // fp8: O is kept in units of the current key tile's V descale: before
-            // P(t) V8(t) is added, O *= alpha * dv(t-1) / dv(t).
+            // P(t) V8(t) is added, O *= alpha * dv(t-1) / dv(t).  When every V block scale
+            // is a power of two (v_pow2), O is kept in units of the largest V scale seen so
+            // far instead, dv_ref, and tile t's ratio dv(t) / dv_ref = 2^k (k <= 0, exact)
+            // goes into P's exponent: P = e4m3(p * 2^(P8_SHIFT + k)).  O is then rescaled only
+            // when the row max or dv_ref grows.
             float dv_cur = 1.0f, q_desc = 1.0f;
             if constexpr (F8) q_desc = p.dq[(size_t)w.z * ((p.N + 127) / 128) + a / 128];
 
@@ -506,13 +510,26 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 const int c0 = t * C::BN;
                 const int sb = (C::NQ == 2) ? grp : (jj & 1);
                 float c = p.c_log2;
-                float dv_ratio = 1.0f;  // fp8: dv(t-1) / dv(t)
+                float dv_ratio = 1.0f;  // fp8: factor on O before P(t) V8(t) is added
+                int pshift = 0;          // fp8, v_pow2: k = log2(dv(t) / dv_ref) <= 0
+                bool dv_up = false;      // fp8, v_pow2: dv_ref grew at this tile
                 if constexpr (F8) {
                     const int nkb = (p.N + 127) / 128;
                     c = p.c_log2 * q_desc * p.dk[(size_t)w.z * nkb + t];
                     const float dv_t = p.dv[(size_t)w.z * nkb + t];
-                    dv_ratio = dv_cur / dv_t;
-                    dv_cur = dv_t;
+                    if (!p.v_pow2) {
+                        dv_ratio = dv_cur / dv_t;
+                        dv_cur = dv_t;
+                    } else if (jj == L || dv_t > dv_cur) {
+                        dv_ratio = (jj == L) ? 1.0f : dv_cur / dv_t;  // O is empty on the first step
+                        dv_up = jj > L;
+                        dv_cur = dv_t;
+                    } else {
+                        // both are powers of two: the exponent difference is exact
+                        pshift = (int)((__float_as_uint(dv_t) >> 23) & 0xFFu) -
+                                 (int)((__float_as_uint(dv_cur) >> 23) & 0xFFu);
+                        pshift = max(pshift, -100);  // P underflows to 0 long before
+                    }
                 }
                 if (!wait_all(&bars->s_full[sb], (s_phase >> sb) & 1)) break;
                 s_phase ^= 1u << sb;
@@ -565,7 +582,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 // P = 2^(s*c - m) (fp8: times 2^P8_SHIFT, folded into the exponent)
                 const float mb = (m_used == NEG_INF) ? 0.0f : m_used;
                 const float2 c2 = make_float2(c, c);
-                const float bias = F8 ? float(C::P8_SHIFT) - mb : -mb;
+                const float bias = F8 ? float(C::P8_SHIFT + pshift) - mb : -mb;
                 const float2 b2 = make_float2(bias, bias);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -606,7 +623,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 const float2 a01 = __fadd2_rn(acc[0], acc[1]);
                 const float2 a23 = __fadd2_rn(acc[2], acc[3]);
                 float rowsum = (a01.x + a01.y) + (a23.x + a23.y);
-                if constexpr (F8) rowsum *= 1.0f / float(1u << C::P8_SHIFT);
+                if constexpr (F8)   // undo the 2^(P8_SHIFT + k) of P (an exact power of two)
+                    rowsum *= __uint_as_float((uint32_t)(127 - C::P8_SHIFT - pshift) << 23);
                 l += rowsum;
 
                 if (jj > L) {
@@ -618,7 +636,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                         if (!wait_all(&bars->pv_done[grp], (pv_phase >> grp) & 1)) break;
                         pv_phase ^= 1u << grp;
                     }
-                    const bool any_resc = F8 ? true : __any_sync(0xffffffffu, resc);
+                    const bool any_resc = (F8 && !p.v_pow2) ? true : (__any_sync(0xffffffffu, resc) || dv_up);
                     if (any_resc) {
                         tc_fence_after_sync();
                         const float f = alpha * dv_ratio;

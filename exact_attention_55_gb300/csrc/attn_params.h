@@ -29,6 +29,7 @@ struct FwdParams {
     float c_log2;         // softmax scale * log2(e)
     unsigned long long timeout_ns;  // bound on every mbarrier wait
     int qk_fmt;           // fp8 path: format of the Q and K codes, 0 E4M3, 1 E5M2 (V is E4M3)
+    int v_pow2;           // fp8 path: V's block scales are powers of two (see the softmax)
     // Packed variable-length sequences (null cu_seqlens: the batched [BH, N, D] layout).
     // q, k, v, o are [T, H, D]; lse is [H, T]; sequence s is tokens [cu[s], cu[s+1]).
     // Units are (sequence, head, pair of query blocks) with num_qblk from max_seqlen.
@@ -88,7 +89,8 @@ struct QuantParams {
     int BH, N, d;
     int nblk;             // ceil(N / 128)
     int rotate;           // 1: Walsh-Hadamard rotation of each row before quantising
-    int fmt;              // 0: E4M3 codes, scale = amax / 448; 1: E5M2, scale = amax / 57344
+    int fmt;              // 0: E4M3 codes, scale = amax / 448; 1: E5M2, scale = amax / 57344;
+                          // 2: E4M3, scale = the smallest power of two >= amax / 448
     float rot_c;          // rotation normalisation fp32(1 / sqrt(d))
 };
 

@@ -10,7 +10,9 @@
 //   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 quotient, one rounding to E4M3)
 // The E5M2 variant (the pages' wider-range format, "大模型加速-核心网络算子-Flash
 // Attention V3" §1.5) divides amax by 57344, its largest finite value, and rounds
-// the same quotient to E5M2.
+// the same quotient to E5M2.  The power-of-two variant keeps E4M3 codes but takes the
+// smallest power of two at or above amax / 448 as the block's scale (a shared exponent),
+// so that the quotient is exact and ratios of two blocks' scales are powers of two.
 //
 // HBM-bound design: persistent CTAs, as many per SM as fit (two at d = 128),
 // each stream whole blocks (one contiguous run of rows * d * 2 bytes) into a
@@ -107,7 +109,18 @@ template <int DR> struct QuantShape {
 };
 
 // DR = 0: plain per-block quantisation (any d); DR = d in {64, 128, 256}: rotate first.
-// FMT = 0: E4M3; FMT = 1: E5M2 (plain quantisation only).
+// FMT = 0: E4M3; FMT = 1: E5M2; FMT = 2: E4M3 with power-of-two scales (plain only).
+
+// The smallest power of two >= s (s > 0 finite), normal or subnormal.
+__device__ __forceinline__ float pow2_at_least(float s)
+{
+    const uint32_t b = __float_as_uint(s);
+    if ((b & 0x7F800000u) == 0) {  // subnormal: 2^k >= m * 2^-149 from m's highest bit
+        const uint32_t m = b & 0x7FFFFFu;
+        return __uint_as_float((m & (m - 1)) == 0 ? m : (1u << (32 - __clz(m))));
+    }
+    return (b & 0x7FFFFFu) == 0 ? s : __uint_as_float((b & 0x7F800000u) + 0x00800000u);
+}
 template <int DR, int FMT = 0>
 __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMinBlocks)
     quant_fp8_kernel(const QuantParams p)
@@ -182,10 +195,11 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
             }
             amax = block_amax(amax);
-            scale = (amax > 0.0f) ? __fdiv_rn(amax, FMT ? 57344.0f : 448.0f) : 1.0f;
+            scale = (amax > 0.0f) ? __fdiv_rn(amax, FMT == 1 ? 57344.0f : 448.0f) : 1.0f;
+            if (FMT == 2 && amax > 0.0f) scale = pow2_at_least(scale);
             const float y = __frcp_rn(scale);
             auto pack2 = [](float lo, float hi) -> uint32_t {
-                return FMT ? pack_e5m2x2(lo, hi) : pack_e4m3x2(lo, hi);
+                return FMT == 1 ? pack_e5m2x2(lo, hi) : pack_e4m3x2(lo, hi);
             };
 
             uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
@@ -336,7 +350,11 @@ static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream)
 {
-    if (!p.rotate) return p.fmt ? launch_quant<0, 1>(p, sm_count, stream) : launch_quant<0, 0>(p, sm_count, stream);
+    if (!p.rotate) {
+        if (p.fmt == 1) return launch_quant<0, 1>(p, sm_count, stream);
+        if (p.fmt == 2) return launch_quant<0, 2>(p, sm_count, stream);
+        return launch_quant<0, 0>(p, sm_count, stream);
+    }
     if (p.fmt) return cudaErrorInvalidValue;    // the rotated variant writes E4M3 only
     switch (p.d) {
     case 64: return launch_quant<64>(p, sm_count, stream);

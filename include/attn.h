@@ -44,8 +44,9 @@ typedef enum {
 } attn_status_t;
 
 /* FP8 formats ([JJ] §1.5 低精度FP8: E4M3, 4 exponent / 3 mantissa bits, largest 448;
- * E5M2, 5 exponent / 2 mantissa bits, largest 57344 -- wider range, less precision). */
-typedef enum { ATTN_FP8_E4M3 = 0, ATTN_FP8_E5M2 = 1 } attn_fp8_format_t;
+ * E5M2, 5 exponent / 2 mantissa bits, largest 57344 -- wider range, less precision).
+ * ATTN_FP8_E4M3_POW2: E4M3 codes whose per-block scale is a power of two. */
+typedef enum { ATTN_FP8_E4M3 = 0, ATTN_FP8_E5M2 = 1, ATTN_FP8_E4M3_POW2 = 2 } attn_fp8_format_t;
 
 /*
  * attn_fwd_bf16 -- O = softmax(scale * Q K^T + mask) V and LSE, bf16 in / bf16 out.
@@ -211,6 +212,9 @@ attn_status_t attn_quantize_fp8_hadamard(const void* x, void* x8, float* scales,
  * format ATTN_FP8_E4M3: exactly attn_quantize_fp8_blockwise.  format ATTN_FP8_E5M2
  * ([JJ] §1.5 and [WGC] §3 name both formats): scale = amax / 57344 (IEEE fp32; 1 when
  * amax == 0) and x8 = E5M2(x / scale), round-to-nearest-even, saturating to +-57344.
+ * format ATTN_FP8_E4M3_POW2 ([WGC] §3 asks only for a per-block scale): E4M3 codes with
+ * scale = the smallest power of two >= fp32(amax / 448), so x / scale is exact; used for V
+ * it lets attn_fwd_fp8_fmt fold the ratio of two blocks' scales into P exactly.
  * Arguments as attn_quantize_fp8_blockwise; another format is ATTN_ERR_INVALID_ARG.
  */
 attn_status_t attn_quantize_fp8_blockwise_fmt(const void* x, void* x8, float* scales, int B,
@@ -238,20 +242,24 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                            int d, float scale, int causal, int window, void* stream);
 
 /*
- * attn_fwd_fp8_fmt -- attn_fwd_fp8 with a choice of format for Q and K.
+ * attn_fwd_fp8_fmt -- attn_fwd_fp8 with a choice of formats.
  *
  * Mixed FP8 formats ([JJ] §1.5: E5M2 trades precision for range): q8 and k8 are both
- * qk_format codes (ATTN_FP8_E4M3 or ATTN_FP8_E5M2, from
- * attn_quantize_fp8_blockwise_fmt), v8 is E4M3, and P is rounded to E4M3 as in
- * attn_fwd_fp8, so each of the two matmuls multiplies two operands of one format.
- * qk_format ATTN_FP8_E4M3 is exactly attn_fwd_fp8.  Other arguments and errors as
- * attn_fwd_fp8; another qk_format is ATTN_ERR_INVALID_ARG.
+ * qk_format codes (ATTN_FP8_E4M3, ATTN_FP8_E5M2 or ATTN_FP8_E4M3_POW2, from
+ * attn_quantize_fp8_blockwise_fmt), v8 is E4M3 (v_format ATTN_FP8_E4M3) or E4M3 with
+ * power-of-two block scales (ATTN_FP8_E4M3_POW2), and P is rounded to E4M3 as in
+ * attn_fwd_fp8, so each of the two matmuls multiplies two operands of one type.  With
+ * power-of-two V scales the kernel applies V's descale through P's exponent and rescales
+ * the O accumulator only when a row's max or the largest V scale so far grows, instead
+ * of on every key tile; v_format ATTN_FP8_E4M3_POW2 with other scales gives wrong results.
+ * qk_format = v_format = ATTN_FP8_E4M3 is exactly attn_fwd_fp8.  Other arguments and
+ * errors as attn_fwd_fp8; another format is ATTN_ERR_INVALID_ARG.
  */
 attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const void* v8,
                                const float* descale_q, const float* descale_k,
                                const float* descale_v, void* o, float* lse, int B, int H, int N,
                                int d, float scale, int causal, int window, int qk_format,
-                               void* stream);
+                               int v_format, void* stream);
 
 /* Static English text for a status code (never NULL). */
 const char* attn_status_string(attn_status_t status);
