@@ -9,9 +9,11 @@
 // 的关键技术实践" §2.3.2: micro-batches' forward and backward passes overlapped in
 // pipeline training, and its introduction: training as well as inference; "大模型加速-
 // 核心网络算子-Flash Attention V3" §2.3-2.4 call the kernel they describe the forward
-// pass); the formulas are the chain rule through the forward definition.  Three launches, no atomics and no fp32 accumulation buffer:
+// pass); the formulas are the chain rule through the forward definition.
+//
+// Three launches, no atomics and no fp32 accumulation buffer:
 //   bwd_dot_kernel          D_i, one warp per row;
-//   bwd_kernel<D, true>     (dQ pass) per 128-row query tile, in steps of 64 keys:
+//   bwd_kernel<D, true>     (dQ pass) per 128-row query tile, in steps of 128 keys:
 //                           S = Q K_j^T and dP = dO V_j^T into TMEM, the compute
 //                           warpgroups turn them into dS (bf16, over S), then
 //                           dQ += dS K_j with K_j as the MN-major operand;
@@ -21,11 +23,13 @@
 // S is recomputed in both passes (7 matmuls per tile pair instead of 5) to keep dQ in
 // TMEM rather than in a global fp32 buffer updated by atomics.
 //
-// Software pipeline: S and dP of a step live in one of two TMEM buffers, so the MMA
-// warp issues step h's S and dP before step h-1's accumulation and the tensor pipe
-// computes them while a compute warpgroup turns step h-1 into P and dS.  The two
-// compute warpgroups ping-pong: warpgroup b takes the steps of buffer b (every other
-// step), so each has two steps' worth of tensor time for its own.
+// Software pipelines.  dQ pass: S(j) goes to one of two TMEM S buffers and dP(j) to one
+// dP buffer that the compute warps release as soon as they have loaded it, so the MMA
+// warp issues dP(j), then the accumulation of step j-1, then S(j+1), and the tensor pipe
+// computes dP(j) and S(j+1) while both compute warpgroups work on steps j-1 and j (64 keys
+// each).  dK/dV pass: S^T and dP^T of a 64-query step live in one of two TMEM step buffers,
+// the MMA warp issues step h's products before step h-1's accumulations, and the two
+// compute warpgroups ping-pong over the buffers (warpgroup b takes the steps of buffer b).
 //
 // Roles per CTA (persistent over units): warps 0-7 compute (two warpgroups, one thread
 // per tile row), warp 8 streams tiles with TMA through an mbarrier ring, warp 9 issues
