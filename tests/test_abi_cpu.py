@@ -128,3 +128,49 @@ def test_missing_library_fails_loudly(tmp_path):
             fa.load_library(str(tmp_path / "nope.so"))
     finally:
         fa._lib = saved
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((P, P, P, 1, 1, 128, 128, 128, 3), 1),       # unknown format
+    ((P, P, P, 1, 1, 128, 128, 128, -1), 1),
+    ((P, P, P, 1, 1, 128, 128, 64, 1), 2),        # E5M2, block != 128
+    ((P + 4, P, P, 1, 1, 128, 128, 128, 2), 3),   # power-of-two scales, x misaligned
+])
+def test_quantizer_fmt_argument_errors(lib, args, expected):
+    assert lib.attn_quantize_fp8_blockwise_fmt(*args, None) == expected
+
+
+@pytest.mark.parametrize("fmts,shape,expected", [
+    ((3, 0), (256, 128), 1),      # unknown Q/K format
+    ((0, 1), (256, 128), 1),      # V in E5M2 is not a V format
+    ((1, 3), (256, 128), 1),
+    ((1, 0), (200, 128), 2),      # E5M2 Q/K, N % 128
+    ((0, 2), (256, 64), 2),       # power-of-two V, d = 64
+])
+def test_fp8_fmt_argument_errors(lib, fmts, shape, expected):
+    N, d = shape
+    args = (P, P, P, P, P, P, P, P, 1, 1, N, d, 0.1, 0, 0)
+    assert lib.attn_fwd_fp8_fmt(*args, *fmts, None) == expected
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.attn_bwd_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 4
+
+
+@pytest.mark.parametrize("change,expected", [
+    ({0: 0}, 1),                  # null q
+    ({9: 0}, 1),                  # null workspace
+    ({10: 4}, 1),                 # workspace too small
+    ({14: 256}, 2),               # d = 256
+    ({14: 96}, 2),
+    ({11: 0}, 1),                 # B = 0
+    ({15: 0.0}, 1),               # scale = 0
+    ({3: P + 2}, 3),              # o misaligned
+    ({5: P + 2}, 3),              # lse misaligned
+])
+def test_bwd_argument_errors(lib, change, expected):
+    # q, k, v, o, dout, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, window
+    args = [P, P, P, P, P, P, P, P, P, P, 1 * 1 * 256 * 4, 1, 1, 256, 128, 0.1, 0, 0]
+    for i, v in change.items():
+        args[i] = v
+    assert lib.attn_bwd_bf16(*args, None) == expected
