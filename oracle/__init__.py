@@ -38,6 +38,8 @@ Functions and the passage each follows:
                              mention for training: [YT] §2.3.2 流水线并行, forward and
                              backward of micro-batches; [JJ] §2.3-2.4 call their
                              kernel the forward pass): dQ, dK, dV of sum(dO * O)
+  attn_varlen_bwd_f64        the backward pass over packed variable-length sequences
+                             (attn_bwd_f64 of each sequence on its own)
   attn_decode_paged_f64      a decoding step against a paged KV cache ([JJ] §3 总结:
                              tokens generated one at a time over cached K/V; [WGC]
                              §局限性与后续方向 item 2: PagedAttention KV-cache management)
@@ -194,6 +196,27 @@ def attn_varlen_f64(q, k, v, cu_seqlens, scale: float, causal: bool = False, win
         o[a:b] = oh.transpose(1, 0, 2)
         lse[:, a:b] = lh
     return o, lse
+
+
+def attn_varlen_bwd_f64(q, k, v, do, cu_seqlens, scale: float, causal: bool = False,
+                        window: int = 0):
+    """Backward pass over packed variable-length sequences ([T, H, d] tensors and
+    cu_seqlens as attn_varlen_f64): attn_bwd_f64 of each sequence on its own.  Returns
+    (dQ, dK, dV) float64 [T, H, d]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    T = q.shape[0]
+    if cu[0] != 0 or cu[-1] != T or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise from 0 to T")
+    out = [np.zeros_like(q) for _ in range(3)]
+    for a, b in zip(cu, cu[1:]):
+        if b == a:
+            continue
+        g = attn_bwd_f64(*(x[a:b].transpose(1, 0, 2) for x in (q, k, v, do)), scale,
+                         causal=causal, window=window)
+        for o_, g_ in zip(out, g):
+            o_[a:b] = g_.transpose(1, 0, 2)
+    return tuple(out)
 
 
 def attn_bwd_f64(q, k, v, do, scale: float, causal: bool = False, window: int = 0):

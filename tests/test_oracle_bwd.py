@@ -81,3 +81,44 @@ def test_closed_forms():
     # causal row 0 sees only key 0: its query gets no gradient
     dq3, _, _ = oracle.attn_bwd_f64(rng.standard_normal((N, d)), k, v, do, 0.5, causal=True)
     np.testing.assert_allclose(dq3[0], 0.0, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,window", MODES)
+def test_varlen_matches_autograd_over_the_packed_tensor(causal, window):
+    """Library special case: autograd through float64 SDPA over the whole packed tensor
+    with the block-diagonal (and causal / window) mask built from the definition."""
+    lengths = [5, 1, 17, 0, 9]
+    H, d = 2, 4
+    rng = np.random.default_rng(21)
+    T = sum(lengths)
+    q, k, v, do = (rng.standard_normal((T, H, d)) for _ in range(4))
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    got = oracle.attn_varlen_bwd_f64(q, k, v, do, cu, 0.4, causal=causal, window=window)
+    seq = np.repeat(np.arange(len(lengths)), lengths)
+    pos = np.concatenate([np.arange(n) for n in lengths])
+    i, j = pos[:, None], pos[None, :]
+    allowed = seq[:, None] == seq[None, :]
+    if causal:
+        allowed &= j <= i
+    if window > 0:
+        allowed &= j >= i - window
+        if not causal:
+            allowed &= j <= i + window
+    tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2), requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(allowed),
+                                                         scale=0.4)
+    o.backward(torch.from_numpy(do.transpose(1, 0, 2)))
+    for g, t in zip(got, (tq, tk, tv)):
+        np.testing.assert_allclose(g, t.grad.numpy().transpose(1, 0, 2), rtol=0, atol=1e-12)
+
+
+def test_varlen_equal_lengths_match_the_batched_layout():
+    B, H, N, d = 3, 2, 11, 4
+    rng = np.random.default_rng(22)
+    q, k, v, do = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    ref = oracle.attn_bwd_f64(q, k, v, do, 0.3, causal=True)
+    pack = lambda x: x.transpose(0, 2, 1, 3).reshape(B * N, H, d)
+    got = oracle.attn_varlen_bwd_f64(pack(q), pack(k), pack(v), pack(do), np.arange(B + 1) * N, 0.3,
+                                     causal=True)
+    for g, r in zip(got, ref):
+        np.testing.assert_array_equal(g, pack(r))
