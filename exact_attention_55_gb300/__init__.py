@@ -27,7 +27,7 @@ from . import build as _build
 
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_TIMEOUT", "load_library", "attn_fwd_bf16",
-    "attn_bwd_bf16", "attn_bwd_workspace_bytes",
+    "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_bwd_bf16_varlen",
     "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_bf16_paged_noalloc",
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
@@ -52,7 +52,8 @@ _FP8_FORMATS = {"e4m3": ATTN_FP8_E4M3, "e5m2": ATTN_FP8_E5M2, "e4m3_pow2": ATTN_
                 ATTN_FP8_E4M3_POW2: ATTN_FP8_E4M3_POW2}
 
 EXPORTED_SYMBOLS = (
-    "attn_fwd_bf16", "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_fwd_bf16_varlen",
+    "attn_fwd_bf16", "attn_bwd_bf16", "attn_bwd_workspace_bytes", "attn_bwd_bf16_varlen",
+    "attn_fwd_bf16_varlen",
     "attn_decode_bf16_paged",
     "attn_decode_bf16_paged_noalloc", "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_blockwise_fmt",
@@ -96,6 +97,9 @@ def load_library(path: str | None = None):
         lib.attn_bwd_bf16.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i,
                                       i, i, f, i, i, vp]
         lib.attn_bwd_bf16.restype = i
+        lib.attn_bwd_bf16_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                             vp, i, i, i, i, i, f, i, i, vp]
+        lib.attn_bwd_bf16_varlen.restype = i
         lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_bf16_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
@@ -210,6 +214,42 @@ def attn_bwd_bf16(q, k, v, o, dout, lse, scale: float | None = None, causal: boo
         workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
         int(bool(causal)), int(window), _stream_handle(stream))
     _raise_if(st, "attn_bwd_bf16")
+    return dq, dk, dv
+
+
+def attn_bwd_bf16_varlen(q, k, v, o, dout, lse, cu_seqlens, max_seqlen: int,
+                         scale: float | None = None, causal: bool = False, window: int = 0,
+                         dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward over packed sequences: returns (dQ, dK, dV) bf16 [T, H, d] for the upstream
+    gradient dout, given attn_fwd_bf16_varlen's o and lse ([H, T]) with the same offsets."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous bf16 CUDA tensor [T, H, d]")
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have q's shape")
+    T, H, d = q.shape
+    _check_out(lse, (H, T), torch.float32, q.device, "lse")
+    if (not cu_seqlens.is_cuda or cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1
+            or not cu_seqlens.is_contiguous()):
+        raise TypeError("cu_seqlens must be a contiguous int32 CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_out(t, (T, H, d), torch.bfloat16, q.device, n)
+    if workspace is None:
+        workspace = torch.empty((H, max(T, 1)), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    st = load_library().attn_bwd_bf16_varlen(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), cu_seqlens.data_ptr(),
+        cu_seqlens.numel() - 1, int(max_seqlen), T, H, d, float(scale), int(bool(causal)),
+        int(window), _stream_handle(stream))
+    _raise_if(st, "attn_bwd_bf16_varlen")
     return dq, dk, dv
 
 

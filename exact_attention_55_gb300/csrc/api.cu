@@ -525,6 +525,71 @@ extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N)
     return (size_t)B * H * N * sizeof(float);
 }
 
+extern "C" attn_status_t attn_bwd_bf16_varlen(const void* q, const void* k, const void* v,
+                                             const void* o, const void* dout, const float* lse,
+                                             void* dq, void* dk, void* dv, void* workspace,
+                                             size_t workspace_bytes, const int* cu_seqlens,
+                                             int num_seqs, int max_seqlen, int total_tokens, int H,
+                                             int d, float scale, int causal, int window,
+                                             void* stream)
+{
+    if (num_seqs < 1 || H < 1 || total_tokens < 0 || max_seqlen < 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)num_seqs * H > 0x7fffffffLL || max_seqlen > total_tokens)
+        return ATTN_ERR_INVALID_ARG;
+    if (total_tokens == 0 || max_seqlen == 0) return ATTN_OK;  // nothing to compute
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace || !cu_seqlens)
+        return ATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < (size_t)H * total_tokens * sizeof(float)) return ATTN_ERR_INVALID_ARG;
+    const long long BH = (long long)num_seqs * H;
+    const long long nt = (max_seqlen + 127) / 128;
+    if (BH * 2 * ((nt + 1) / 2) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;  // sub-units fit an int
+    if ((long long)total_tokens * H > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 4) || !aligned(cu_seqlens, 4))
+        return ATTN_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // [T, H, d] maps: 128-token boxes for a unit's fixed tiles, 64-token boxes for the ring
+    alignas(64) BwdMaps maps;
+    const void* src[4] = {q, k, v, dout};
+    CUtensorMap* big[4] = {&maps.q, &maps.k, &maps.v, &maps.dout};
+    CUtensorMap* small[4] = {&maps.q64, &maps.k64, &maps.v64, &maps.dout64};
+    for (int i = 0; i < 4; ++i)
+        if (!encode_3d_packed(big[i], src[i], dt, 2, d, H, total_tokens, 128) ||
+            !encode_3d_packed(small[i], src[i], dt, 2, d, H, total_tokens, 64))
+            return ATTN_ERR_CUDA;
+    BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.o = o;
+    p.dout = dout;
+    p.lse = lse;
+    p.delta = static_cast<float*>(workspace);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = dev->status;
+    p.BH = (int)BH;
+    p.N = max_seqlen;
+    p.nt = (int)nt;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    p.scale = scale;
+    p.timeout_ns = kWaitTimeoutNs;
+    p.cu_seqlens = cu_seqlens;
+    p.num_seqs = num_seqs;
+    p.H = H;
+    p.T = total_tokens;
+    if (launch_bwd(maps, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
 extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
                                       const void* dout, const float* lse, void* dq, void* dk,
                                       void* dv, void* workspace, size_t workspace_bytes, int B,

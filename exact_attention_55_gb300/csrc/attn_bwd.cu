@@ -110,15 +110,37 @@ __device__ __forceinline__ void bwd_timeout(const BwdParams& p, BwdBars* bars)
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
 }
 
-// Steps (blocks of `bc` columns of the other operand, bc = 128 or 64) that tile t (rows
-// [128 t, 128 t + 128)) meets under the mask: for a query tile, the key blocks [lo, hi);
-// for a key tile (transposed), the query blocks.  Computed on 128-column tiles, then (bc
-// = 64) split in two and cut at the sequence end.
-__device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_tile, int bc, int& lo, int& hi)
+// One unit of work: tile t of one head of one sequence, with where its rows live.
+// Batched layout: head bh, rows r at TMA coordinates (r, bh), LSE / D at bh N + r, output
+// row bh N + r.  Packed sequences: head h of tokens [y0, y0 + N), row r at TMA coordinates
+// (h, y0 + r), LSE / D at h T + y0 + r, output row (y0 + r) H + h.
+struct BwdUnit {
+    int t;            // tile (128 rows) within the sequence
+    int N;            // rows of the sequence
+    int c1, c2;       // TMA coordinates of row 0: (row offset, head) or (head, token)
+    bool packed;
+    size_t vbase;     // LSE / D index of row 0
+    size_t obase;     // output row index of row 0
+    int ostride;      // output rows between consecutive sequence rows
+};
+
+__device__ __forceinline__ void bwd_coords(const BwdUnit& u, int r, int& c1, int& c2)
 {
-    const int a = t * 128, last = min(p.N, a + 128) - 1;
+    c1 = u.packed ? u.c1 : u.c1 + r;
+    c2 = u.packed ? u.c2 + r : u.c2;
+}
+
+// Steps (blocks of `bc` columns of the other operand, bc = 128 or 64) that tile t (rows
+// [128 t, 128 t + 128)) of a sequence of N rows meets under the mask: for a query tile,
+// the key blocks [lo, hi); for a key tile (transposed), the query blocks.  Computed on
+// 128-column tiles, then (bc = 64) split in two and cut at the sequence end.
+__device__ __forceinline__ void bwd_steps(const BwdParams& p, const BwdUnit& u, bool key_tile, int bc,
+                                          int& lo, int& hi)
+{
+    const int t = u.t, N = u.N;
+    const int a = t * 128, last = min(N, a + 128) - 1;
     lo = 0;
-    hi = p.nt;
+    hi = (N + 127) / 128;
     if (!key_tile) {
         if (p.causal) hi = min(hi, last / 128 + 1);
         else if (p.window > 0) hi = min(hi, (last + p.window) / 128 + 1);
@@ -132,7 +154,7 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_ti
     if (lo >= hi) hi = lo + 1;  // never empty (cannot happen for the masks above)
     if (bc == 64) {
         lo *= 2;
-        hi = min(2 * hi, (p.N + 63) / 64);
+        hi = min(2 * hi, (N + 63) / 64);
     }
 }
 
@@ -143,15 +165,39 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, int t, bool key_ti
 // whose costs add up to the same nt + 1 tiles for every k; a CTA takes both halves of a
 // pair, pairs go round-robin, and pairs of one head are adjacent so CTAs that run at the
 // same time share that head's operands in L2.  Sub-unit s is half (s & 1) of pair s >> 1;
-// the middle tile of an odd tile count appears once.
-__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, int& bh, int& t)
+// the middle tile of an odd tile count appears once.  Packed sequences: pair slots are
+// laid out for the longest sequence and a shorter one skips the slots it does not have;
+// offsets are clamped to [0, T] so a unit never addresses a token outside the tensors.
+template <bool kPacked>
+__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u)
 {
     const int npair = (p.nt + 1) >> 1;
     const int pair = s >> 1;
-    bh = pair / npair;
-    const int k = pair - bh * npair;
-    t = (s & 1) ? k : p.nt - 1 - k;
-    return !((s & 1) && k == p.nt - 1 - k);
+    const int sh = pair / npair;                 // batched: bh; packed: sequence * H + head
+    const int k = pair - sh * npair;
+    u.packed = kPacked;
+    if (!u.packed) {
+        u.N = p.N;
+        u.c1 = 0;
+        u.c2 = sh;
+        u.vbase = (size_t)sh * p.N;
+        u.obase = (size_t)sh * p.N;
+        u.ostride = 1;
+    } else {
+        const int seq = sh / p.H, h = sh - seq * p.H;
+        const int a = min(max(__ldg(p.cu_seqlens + seq), 0), p.T);
+        const int b = min(max(__ldg(p.cu_seqlens + seq + 1), a), p.T);
+        u.N = b - a;
+        u.c1 = h;
+        u.c2 = a;
+        u.vbase = (size_t)h * p.T + a;
+        u.obase = (size_t)a * p.H + h;
+        u.ostride = p.H;
+    }
+    const int nt = (u.N + 127) / 128;
+    if (k >= ((nt + 1) >> 1)) return false;      // beyond this sequence's pairs (or empty)
+    u.t = (s & 1) ? k : nt - 1 - k;
+    return !((s & 1) && k == nt - 1 - k);
 }
 
 __device__ __forceinline__ int bwd_next(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
@@ -161,9 +207,9 @@ __device__ __forceinline__ int bwd_next(int s) { return (s & 1) ? s + 2 * (int)g
 // no per-element test: causal needs the last key at or before the first query, a window
 // the first key within w of the last query (and, without causal, the last key within
 // w after the first query).
-__device__ __forceinline__ bool bwd_block_full(const BwdParams& p, int q0, int nq, int k0, int nk)
+__device__ __forceinline__ bool bwd_block_full(const BwdParams& p, int N, int q0, int nq, int k0, int nk)
 {
-    if (q0 + nq > p.N || k0 + nk > p.N) return false;
+    if (q0 + nq > N || k0 + nk > N) return false;
     if (p.causal && k0 + nk - 1 > q0) return false;
     if (p.window > 0) {
         if (k0 < q0 + nq - 1 - p.window) return false;
@@ -179,7 +225,9 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const BwdParams p)
     constexpr int E = D / 32;
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= (long long)p.BH * p.N) return;
+    // batched: rows bh N + r, D at the same index; packed: rows token H + h, D at h T + token
+    const long long nrows = p.cu_seqlens ? (long long)p.T * p.H : (long long)p.BH * p.N;
+    if (row >= nrows) return;
     const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o) + row * D + lane * E;
     const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D + lane * E;
     float acc = 0.0f;
@@ -187,14 +235,14 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const BwdParams p)
     for (int e = 0; e < E; ++e) acc = fmaf(__bfloat162float(o[e]), __bfloat162float(g[e]), acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) p.delta[row] = acc;
+    if (lane == 0) p.delta[p.cu_seqlens ? (row % p.H) * p.T + row / p.H : row] = acc;
 }
 
-// One pass.  `kDQ` selects it: the dQ pass's unit is a query tile (fixed tiles Q, dO;
+// One pass (kPacked: packed variable-length sequences).  `kDQ` selects it: the dQ pass's unit is a query tile (fixed tiles Q, dO;
 // ring V then K of each 128-key step, 128-row boxes), the dK/dV pass's unit is a key tile
 // (fixed tiles K, V; ring Q then dO of each 64-query step, 64-row boxes).  The fixed maps
 // have 128-row boxes.
-template <int D, bool kDQ>
+template <int D, bool kDQ, bool kPacked>
 __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmFixA, const __grid_constant__ CUtensorMap tmFixB,
                const __grid_constant__ CUtensorMap tmRingA, const __grid_constant__ CUtensorMap tmRingB,
@@ -247,10 +295,11 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             uint32_t rc = 0, uc = 0, armed = 0;
             bool ok = true;
             for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
-                int bh, t;
-                if (!bwd_unit(p, su, bh, t)) continue;
+                BwdUnit un;
+                if (!bwd_unit<kPacked>(p, su, un)) continue;
+                const int t = un.t;
                 int lo, hi;
-                bwd_steps(p, t, !kDQ, C::BC, lo, hi);
+                bwd_steps(p, un, !kDQ, C::BC, lo, hi);
                 if (!mbar_wait(smem_u32(&bars->fix_empty), (uc & 1) ^ 1, abort_flag, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -258,11 +307,13 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 const uint32_t fb = smem_u32(&bars->fix_full);
                 mbar_arrive_expect_tx(fb, 2 * C::FIX_BYTES);
                 ++armed;
+                int f1, f2;
+                bwd_coords(un, t * 128, f1, f2);
 #pragma unroll
                 for (int cb = 0; cb < C::NCB; ++cb) {
-                    tma_load_3d(smem_u32(fix + cb * C::FIX_CB), &tmFixA, fb, cb * 64, t * 128, bh, pol_fix);
+                    tma_load_3d(smem_u32(fix + cb * C::FIX_CB), &tmFixA, fb, cb * 64, f1, f2, pol_fix);
                     tma_load_3d(smem_u32(fix + C::FIX_BYTES + cb * C::FIX_CB), &tmFixB, fb, cb * 64,
-                                t * 128, bh, pol_fix);
+                                f1, f2, pol_fix);
                 }
                 for (int s = lo; s < hi && ok; ++s) {
 #pragma unroll
@@ -280,10 +331,11 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                         }
                         const CUtensorMap* map = (which == 0) == kDQ ? &tmRingB : &tmRingA;
                         uint8_t* dst = ring + slot * C::SLOT_BYTES + (kDQ ? 0 : which * C::RING_BYTES);
+                        int r1, r2;
+                        bwd_coords(un, s * C::BC, r1, r2);
 #pragma unroll
                         for (int cb = 0; cb < C::NCB; ++cb)
-                            tma_load_3d(smem_u32(dst + cb * C::RING_CB), map, rb, cb * 64, s * C::BC, bh,
-                                        pol_ring);
+                            tma_load_3d(smem_u32(dst + cb * C::RING_CB), map, rb, cb * 64, r1, r2, pol_ring);
                         if (kDQ || which == 1) ++rc;
                     }
                 }
@@ -346,11 +398,10 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                                    b0 + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
         for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
-            int bh, t;
-            if (!bwd_unit(p, su, bh, t)) continue;
-            (void)bh;
+            BwdUnit un;
+            if (!bwd_unit<kPacked>(p, su, un)) continue;
             int lo, hi;
-            bwd_steps(p, t, false, C::BC, lo, hi);
+            bwd_steps(p, un, false, C::BC, lo, hi);
             const uint32_t r0 = rc, h0 = hs;            // tiles: V_j at r0 + 2(j-lo), K_j next
             if (!wait(&bars->fix_full, uc & 1)) break;
             tc_fence_after_sync();
@@ -442,10 +493,10 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                                    idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
         for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
-            int bh, t;
-            if (!bwd_unit(p, su, bh, t)) continue;
+            BwdUnit un;
+            if (!bwd_unit<kPacked>(p, su, un)) continue;
             int lo, hi;
-            bwd_steps(p, t, !kDQ, C::BC, lo, hi);
+            bwd_steps(p, un, !kDQ, C::BC, lo, hi);
             if (!wait(&bars->fix_full, uc & 1)) break;
             tc_fence_after_sync();
             bool acc_started = false;
@@ -518,23 +569,24 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         // of a step; each warp keeps its own copy in shared memory while it works on it
         float* my_lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512) + warp * 128;
         float* my_delta = my_lse2 + 64;
-        auto col_load = [&](int bh, int c, float2& l2v, float2& dv) {
-            const size_t base = (size_t)bh * p.N;
-            const int c0 = min(c + 2 * lane, p.N - 1), c1 = min(c + 2 * lane + 1, p.N - 1);
+        auto col_load = [&](const BwdUnit& cu, int c, float2& l2v, float2& dv) {
+            const size_t base = cu.vbase;
+            const int c0 = min(c + 2 * lane, cu.N - 1), c1 = min(c + 2 * lane + 1, cu.N - 1);
             l2v = make_float2(__ldg(p.lse + base + c0) * LOG2E, __ldg(p.lse + base + c1) * LOG2E);
             dv = make_float2(__ldg(p.delta + base + c0), __ldg(p.delta + base + c1));
         };
         for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
-            int bh, t;
-            if (!bwd_unit(p, su, bh, t)) continue;
+            BwdUnit un;
+            if (!bwd_unit<kPacked>(p, su, un)) continue;
+            const int t = un.t, NS = un.N;              // tile and sequence length
             int lo, hi;
-            bwd_steps(p, t, !kDQ, C::BC, lo, hi);
+            bwd_steps(p, un, !kDQ, C::BC, lo, hi);
             const int my = t * 128 + trow;              // this thread's row (query or key)
-            const bool valid = my < p.N;
+            const bool valid = my < NS;
             float lse2 = 0.0f, dlt = 0.0f;              // dQ pass: per-row LSE and D
             if constexpr (kDQ) {
-                lse2 = valid ? p.lse[(size_t)bh * p.N + my] * LOG2E : 0.0f;
-                dlt = valid ? p.delta[(size_t)bh * p.N + my] : 0.0f;
+                lse2 = valid ? p.lse[un.vbase + my] * LOG2E : 0.0f;
+                dlt = valid ? p.delta[un.vbase + my] : 0.0f;
             }
             // The columns (the other index) the mask allows for this thread's row form one
             // interval [m_lo, m_hi]: for a query row, keys from i - w (w > 0) or 0 to i
@@ -545,12 +597,12 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             int m_lo, m_hi;
             if constexpr (kDQ) {
                 m_lo = p.window > 0 ? my - p.window : 0;
-                m_hi = p.causal ? my : (p.window > 0 ? my + p.window : p.N - 1);
+                m_hi = p.causal ? my : (p.window > 0 ? my + p.window : NS - 1);
             } else {
                 m_lo = p.causal ? my : (p.window > 0 ? my - p.window : 0);
-                m_hi = p.window > 0 ? my + p.window : p.N - 1;
+                m_hi = p.window > 0 ? my + p.window : NS - 1;
             }
-            m_hi = min(m_hi, p.N - 1);
+            m_hi = min(m_hi, NS - 1);   // packed: the next sequence's tokens in a tile are masked
             const uint32_t m_span = (uint32_t)(m_hi - m_lo);
           if constexpr (kDQ) {
             // dQ pass: both warpgroups work on every step, warpgroup wg on keys
@@ -603,7 +655,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                         tmem_st16p(sb + ch * 16, pk);
                     }
                 };
-                if (bwd_block_full(p, t * 128, 128, j * C::BC, C::BC))
+                if (bwd_block_full(p, NS, t * 128, 128, j * C::BC, C::BC))
                     stepq(std::false_type{});
                 else
                     stepq(std::true_type{});
@@ -618,7 +670,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             int s = lo + (int)((h0 ^ (uint32_t)wg) & 1u);   // this warpgroup's first step
             [[maybe_unused]] float2 nl2 = make_float2(0.f, 0.f), nd = nl2;
             if constexpr (!kDQ) {
-                if (s < hi) col_load(bh, s * C::BC, nl2, nd);
+                if (s < hi) col_load(un, s * C::BC, nl2, nd);
             }
             for (; s < hi; s += 2) {
                 const uint32_t hh = h0 + (uint32_t)(s - lo);
@@ -630,7 +682,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                     *reinterpret_cast<float2*>(my_lse2 + 2 * lane) = nl2;
                     *reinterpret_cast<float2*>(my_delta + 2 * lane) = nd;
                     __syncwarp();
-                    if (s + 2 < hi) col_load(bh, c0 + 2 * C::BC, nl2, nd);
+                    if (s + 2 < hi) col_load(un, c0 + 2 * C::BC, nl2, nd);
                 }
                 if (!wait_all(&bars->s_full[wg], (hh >> 1) & 1)) break;
                 tc_fence_after_sync();
@@ -696,7 +748,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                         }
                     }
                 };
-                if (bwd_block_full(p, kDQ ? t * 128 : c0, kDQ ? 128 : C::BC, kDQ ? c0 : t * 128,
+                if (bwd_block_full(p, NS, kDQ ? t * 128 : c0, kDQ ? 128 : C::BC, kDQ ? c0 : t * 128,
                                    kDQ ? C::BC : 128))
                     step(std::false_type{});
                 else
@@ -717,7 +769,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 const int which = kDQ ? 0 : wg;
                 const float f = kDQ ? p.scale : (which == 0 ? 1.0f : p.scale);
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(kDQ ? p.dq : (which == 0 ? p.dv : p.dk));
-                out += ((size_t)bh * p.N + my) * D;
+                out += (un.obase + (size_t)my * un.ostride) * D;
                 constexpr int NCH = kDQ ? D / 64 : D / 32;     // 32-column chunks per warpgroup
                 const int ch0 = kDQ ? wg * NCH : 0;
 #pragma unroll
@@ -753,19 +805,19 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
     if (warp == C::MMA_WARP) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cudaStream_t stream)
 {
     using CQ = BwdCfg<D, true>;
     using CKV = BwdCfg<D, false>;
-    const long long rows = (long long)p.BH * p.N;
+    const long long rows = p.cu_seqlens ? (long long)p.T * p.H : (long long)p.BH * p.N;
     bwd_dot_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int pairs = ((p.nt + 1) >> 1) * p.BH;     // units go out in pairs (bwd_unit)
     const int grid = pairs < sm_count ? pairs : sm_count;
-    auto kq = bwd_kernel<D, true>;
-    auto kkv = bwd_kernel<D, false>;
+    auto kq = bwd_kernel<D, true, kPacked>;
+    auto kkv = bwd_kernel<D, false, kPacked>;
     if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES)) != cudaSuccess)
         return e;
     if ((e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, CKV::SMEM_BYTES)) != cudaSuccess)
@@ -785,8 +837,11 @@ cudaError_t launch_bwd_t(const BwdMaps& m, const BwdParams& p, int sm_count, cud
 
 cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count, cudaStream_t stream)
 {
-    if (d == 64) return launch_bwd_t<64>(m, p, sm_count, stream);
-    if (d == 128) return launch_bwd_t<128>(m, p, sm_count, stream);
+    const bool packed = p.cu_seqlens != nullptr;
+    if (d == 64) return packed ? launch_bwd_t<64, true>(m, p, sm_count, stream)
+                               : launch_bwd_t<64, false>(m, p, sm_count, stream);
+    if (d == 128) return packed ? launch_bwd_t<128, true>(m, p, sm_count, stream)
+                                : launch_bwd_t<128, false>(m, p, sm_count, stream);
     return cudaErrorInvalidValue;
 }
 

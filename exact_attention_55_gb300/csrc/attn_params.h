@@ -55,6 +55,12 @@ struct BwdParams {
     float c_log2;         // scale * log2(e)
     float scale;
     unsigned long long timeout_ns;
+    // Packed variable-length sequences (null cu_seqlens: the batched layout).  Tensors
+    // are [T, H, D], lse / delta [H, T]; BH = num_seqs * H, N = max_seqlen, nt from N.
+    const int* cu_seqlens;
+    int num_seqs;
+    int H;
+    int T;
 };
 
 // Tensor maps of the backward pass: 128-row boxes for a unit's fixed tiles, 64-row

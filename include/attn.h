@@ -85,6 +85,27 @@ attn_status_t attn_fwd_bf16(const void* q, const void* k, const void* v, void* o
  * Alignment: tensors 16 bytes; lse and workspace 4 bytes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * attn_bwd_bf16_varlen -- attn_bwd_bf16 over packed variable-length sequences, the
+ * backward of attn_fwd_bf16_varlen ([YT] §1.1: variable sequence lengths).
+ *
+ * Every sequence is its own attention problem, as in the forward.
+ *   q, k, v, o, dout : const bf16 [T, H, d] packed; o and lse as attn_fwd_bf16_varlen
+ *                      wrote them (lse float [H, T], natural log)
+ *   dq, dk, dv       : bf16 [T, H, d], written for the tokens of every sequence
+ *   workspace        : device memory of at least attn_bwd_workspace_bytes(1, H, T) bytes
+ *   cu_seqlens       : int32 [num_seqs + 1] on the device, as attn_fwd_bf16_varlen
+ *   max_seqlen       : >= every sequence's length (sizes the work); total_tokens = T
+ *   d in {64, 128}; scale, causal, window as the forward call.  T == 0 returns ATTN_OK.
+ * Offsets are clamped on the device; tokens outside every sequence are not written.
+ */
+attn_status_t attn_bwd_bf16_varlen(const void* q, const void* k, const void* v, const void* o,
+                                   const void* dout, const float* lse, void* dq, void* dk,
+                                   void* dv, void* workspace, size_t workspace_bytes,
+                                   const int* cu_seqlens, int num_seqs, int max_seqlen,
+                                   int total_tokens, int H, int d, float scale, int causal,
+                                   int window, void* stream);
 attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
