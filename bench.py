@@ -513,6 +513,30 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
             "tensor_tflops_executed": t * 7.0 / 5.0,
             "frac_of_peak": t / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))}
     del dout, dqb, dkb, dvb, bws
+    # backward over the packed-sequence workload (131072 tokens, lengths uniform in
+    # [512, 16384], seed 3); FLOPs 10 d per allowed (query, key) pair and head
+    from exact_attention_55_gb300.inputs import make_packed_qkv, varlen_lengths
+    lengths = varlen_lengths(B * N, 512, 16384, seed=3)
+    qp, kp, vp, cu = make_packed_qkv(lengths, H, D, seed=0)
+    qp, kp, vp, cu = qp.to(dev), kp.to(dev), vp.to(dev), cu.to(dev)
+    gen.manual_seed(12)
+    dop = torch.randn(qp.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    dqp, dkp, dvp = torch.empty_like(qp), torch.empty_like(qp), torch.empty_like(qp)
+    wsp = torch.empty((H, qp.shape[0]), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        op, lp = fa.attn_fwd_bf16_varlen(qp, kp, vp, cu, max(lengths), scale=scale, causal=causal,
+                                         stream=stream)
+
+        def bwd_varlen_step():
+            fa.attn_bwd_bf16_varlen(qp, kp, vp, op, dop, lp, cu, max(lengths), scale=scale,
+                                    causal=causal, dq=dqp, dk=dkp, dv=dvp, workspace=wsp, stream=stream)
+        ms, per = time_steps(bwd_varlen_step, reps, 3, stream)
+        f = sum(10.0 * H * D * allowed_pairs(n, causal, 0) for n in lengths)
+        out["bwd_varlen_causal" if causal else "bwd_varlen"] = {
+            "tflops": f / (statistics.mean(per) * 1e-3) / 1e12, "ms": statistics.mean(per),
+            "sequences": len(lengths), "tokens": int(sum(lengths))}
+        del op, lp
+    del qp, kp, vp, cu, dop, dqp, dkp, dvp, wsp
     status = fa.attn_get_device_status()
     out["device_status"] = status
     return out
