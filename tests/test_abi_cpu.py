@@ -174,3 +174,21 @@ def test_bwd_argument_errors(lib, change, expected):
     for i, v in change.items():
         args[i] = v
     assert lib.attn_bwd_bf16(*args, None) == expected
+
+
+@pytest.mark.parametrize("change,expected", [
+    ({14: 0}, 0),                 # zero tokens: nothing to do
+    ({12: 0}, 1),                 # num_seqs = 0
+    ({0: 0}, 1),                  # null q
+    ({11: 0}, 1),                 # null cu_seqlens
+    ({10: 4}, 1),                 # workspace too small
+    ({16: 256}, 2),               # d = 256
+    ({13: 300}, 1),               # max_seqlen > T
+    ({11: P + 2}, 3),             # cu_seqlens misaligned
+])
+def test_bwd_varlen_argument_errors(lib, change, expected):
+    # q, k, v, o, dout, lse, dq, dk, dv, ws, ws_bytes, cu, S, max_seqlen, T, H, d, scale, causal, window
+    args = [P, P, P, P, P, P, P, P, P, P, 2 * 256 * 4, P, 2, 128, 256, 2, 128, 0.1, 0, 0]
+    for i, v in change.items():
+        args[i] = v
+    assert lib.attn_bwd_bf16_varlen(*args, None) == expected
