@@ -177,7 +177,7 @@ def test_bwd_argument_errors(lib, change, expected):
 
 
 @pytest.mark.parametrize("change,expected", [
-    ({14: 0}, 0),                 # zero tokens: nothing to do
+    ({14: 0, 13: 0}, 0),          # zero tokens: nothing to do
     ({12: 0}, 1),                 # num_seqs = 0
     ({0: 0}, 1),                  # null q
     ({11: 0}, 1),                 # null cu_seqlens
