@@ -372,6 +372,38 @@ def run_gb300(args, world, rank, local):
         print(json.dumps(line))
 
 
+def measure_fp8_peak(dev):
+    """Dense FP8 tensor rate of the library GEMM on this GPU: torch._scaled_mm (cuBLASLt)
+    on E4M3 8192^3 with a bf16 output, best of 10 CUDA-event-timed calls after warm-up,
+    plain and fast accumulation (the better of the two).  2 * 8192^3 FLOPs per call."""
+    import torch
+    n = 8192
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    a = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn((n, n), generator=g, device=dev).to(torch.float8_e4m3fn).t()  # column-major
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    best = {}
+    for fast in (False, True):
+        def mm():
+            return torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16, use_fast_accum=fast)
+        for _ in range(3):
+            mm()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record()
+            mm()
+            s1.record()
+            s1.synchronize()
+            times.append(s0.elapsed_time(s1))
+        best["fast_accum" if fast else "plain"] = 2.0 * n ** 3 / (min(times) * 1e-3) / 1e12
+    del a, b
+    return {"tflops": max(best.values()), **best,
+            "how": "torch._scaled_mm e4m3 8192^3 -> bf16, best of 10 (cuBLASLt), burst"}
+
+
 def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     """Causal bf16, the FP8 path and the quantiser on the same device."""
     import torch
@@ -421,8 +453,16 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     out["quantize_fp8_hadamard_qk"] = {"GB_per_s": gbs, "ms_3_tensors": statistics.mean(per),
                                        "frac_of_hbm": gbs / hbm, "bytes": qbytes}
     (q8, sq), (k8, sk), (v8, sv) = bufs
-    peak8 = float(peaks.get("fp8_tflops",
-                            FP8_NOMINAL_RATIO * float(peaks.get("bf16_tflops", 1900.0))))
+    derived8 = FP8_NOMINAL_RATIO * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    try:
+        m8 = measure_fp8_peak(dev)
+    except Exception as exc:  # a library GEMM this torch build cannot run here
+        m8 = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+    out["fp8_peak"] = {**m8, "derived_2x_bf16_burst": derived8}
+    if "tflops" in m8:
+        peak8, src8 = m8["tflops"], "measured: " + m8["how"]
+    else:
+        peak8, src8 = derived8, "derived: 2 x measured bf16 burst (nominal ratio)"
     for causal in (False, True):
         def fp8_step():
             fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, scale=scale, causal=causal, o=o, lse=lse,
@@ -432,7 +472,33 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
         t = f / (statistics.mean(per) * 1e-3) / 1e12
         out["fp8_causal" if causal else "fp8"] = {
             "tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
-            "peak": peak8, "peak_source": "fp8 = 2 x measured bf16 burst (nominal ratio)"}
+            "peak": peak8, "peak_source": src8, "frac_of_derived_2x_bf16": t / derived8}
+    # the specification's FP8 bar against attention on the unquantised inputs,
+    # RMSE(dO)/RMS(O) <= 4e-2, on the whole FP8 workload; the unquantised attention is
+    # this library's bf16 kernel on the same bf16 inputs (itself within the bf16 bars
+    # of the float64 oracle, rel-RMSE ~4e-3)
+    o_fp8 = torch.empty_like(qd)
+    o_ref = torch.empty_like(qd)
+    bars = {}
+    for causal in (False, True):
+        fa.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, scale=scale, causal=causal, o=o_fp8, lse=lse,
+                        stream=stream)
+        fa.attn_fwd_bf16(q2d, k2d, v2d, scale=scale, causal=causal, o=o_ref, lse=lse, stream=stream)
+        torch.cuda.synchronize()
+        err = rel_rmse_dev(o_fp8, o_ref)
+        bars["causal" if causal else "non_causal"] = {"rel_rmse": err, "pass": err <= 4e-2}
+    qh8, sqh = hbufs[0]
+    kh8, skh = hbufs[1]
+    fa.attn_fwd_fp8(qh8, kh8, v8, sqh, skh, sv, scale=scale, causal=False, o=o_fp8, lse=lse,
+                    stream=stream)
+    fa.attn_fwd_bf16(q2d, k2d, v2d, scale=scale, causal=False, o=o_ref, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    err = rel_rmse_dev(o_fp8, o_ref)
+    bars["hadamard_qk_non_causal"] = {"rel_rmse": err, "pass": err <= 4e-2}
+    out["fp8_bar_vs_unquantised"] = {
+        "bar": 4e-2, **bars,
+        "against": "attn_fwd_bf16 on the same (unquantised) bf16 inputs, all 256 heads"}
+    del o_fp8, o_ref
     # mixed FP8 formats: Q and K quantised to E5M2 (amax / 57344), V kept in E4M3
     qe, sqe = fa.attn_quantize_fp8_blockwise_fmt(q2d, "e5m2")
     ke, ske = fa.attn_quantize_fp8_blockwise_fmt(k2d, "e5m2")
@@ -540,6 +606,18 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     status = fa.attn_get_device_status()
     out["device_status"] = status
     return out
+
+
+def rel_rmse_dev(a, ref):
+    """RMSE(a - ref) / RMS(ref) over whole device tensors, accumulated in float64."""
+    import torch
+    num = torch.zeros((), dtype=torch.float64, device=a.device)
+    den = torch.zeros((), dtype=torch.float64, device=a.device)
+    for x, r in zip(a.reshape(64, -1), ref.reshape(64, -1)):
+        r64 = r.double()
+        num += ((x.double() - r64) ** 2).sum()
+        den += (r64 ** 2).sum()
+    return float(torch.sqrt(num / den))
 
 
 def run_profile_case(args):

@@ -63,5 +63,15 @@ def assert_bf16_close(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
     return e
 
 
+def fp8_lse_bound(lse_ref):
+    """Per-row bound on |LSE_kernel - LSE_oracle| for the FP8 path against the oracle
+    on the dequantised inputs: 1e-3 (the specification's LSE bar) relative to
+    max(1, |LSE|).  Both sides see the same dequantised scores; the kernel holds them
+    in fp32 (exact E4M3 products accumulated by the tensor core, then one product
+    with the fp32 descale scale * log2(e) * dq * dk), so its LSE error grows with the
+    score magnitude, which outliers raise to a few hundred on the FP8 workload."""
+    return 1e-3 * np.maximum(1.0, np.abs(lse_ref))
+
+
 def rel_rmse(a, ref):
     return float(np.sqrt(np.mean((a - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))

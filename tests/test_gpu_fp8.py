@@ -7,9 +7,9 @@ import pytest
 import torch
 
 import oracle
-from exact_attention_55_gb300.inputs import make_qkv, sampled_heads, sampled_rows
-from tests.attn_check import (FP8_P_ROUNDING_BOUND, FP8_REL_RMSE_DEQ, gather, oracle_rows,
-                              rel_rmse)
+from exact_attention_55_gb300.inputs import make_qkv, sampled_heads
+from tests.attn_check import (FP8_P_ROUNDING_BOUND, FP8_REL_RMSE_DEQ, fp8_lse_bound, gather,
+                              oracle_rows, rel_rmse)
 from tests.conftest import require_gpu
 
 pytestmark = pytest.mark.gpu
@@ -107,9 +107,12 @@ def _fp8_case(fa, B, H, N, d, causal, window, seed, heads=None, rows=None, outli
     o = o.cpu()
     heads = heads or [(b, h) for b in range(B) for h in range(H)]
     rows = rows if rows is not None else list(range(N))
-    # oracle (ii): the dequantised FP8 inputs the kernel actually consumed
-    deq = [oracle.dequantize(t8.cpu().numpy(), s.cpu().numpy(), 128)
-           for t8, s in ((q8, sq), (k8, sk), (v8, sv))]
+    # oracle (ii): the dequantised FP8 inputs the kernel actually consumed (only the
+    # checked heads are dequantised; the dict is indexed by (b, h) like the tensors)
+    deq = []
+    for t8, s in ((q8, sq), (k8, sk), (v8, sv)):
+        t8c, sc = t8.cpu().numpy(), s.cpu().numpy()
+        deq.append({(b, h): oracle.dequantize(t8c[b, h], sc[b, h], 128) for (b, h) in heads})
     o_deq, lse_deq = oracle_rows(deq[0], deq[1], deq[2], heads, rows, scale, causal, window)
     # oracle (i): the unquantised bf16 inputs
     o_unq, _ = oracle_rows(q, k, v, heads, rows, scale, causal, window)
@@ -121,6 +124,8 @@ def _fp8_case(fa, B, H, N, d, causal, window, seed, heads=None, rows=None, outli
         "vs_unq": rel_rmse(o_g, o_unq),
         "oracle_deq_vs_unq": rel_rmse(o_deq, o_unq),
         "lse_max_abs_vs_deq": float(np.abs(lse_g - lse_deq).max()),
+        "lse_bound_ratio": float((np.abs(lse_g - lse_deq) / fp8_lse_bound(lse_deq)).max()),
+        "rows_checked": int(len(heads) * len(rows)),
     }
 
 
@@ -130,7 +135,7 @@ def test_fp8_attention_small(fa, causal, window):
     assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
     # the rest of the error against the unquantised inputs is the quantiser's
     assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_REL_RMSE_DEQ, e
-    assert e["lse_max_abs_vs_deq"] <= 2e-2, e
+    assert e["lse_bound_ratio"] <= 1.0, e
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -166,11 +171,14 @@ def test_fp8_closed_form_zero_query(fa):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_attention_headline_sampled(fa, causal):
-    """FP8 workload: B=16, H=16, N=8192, d=128 with outliers; 4 heads x 96 rows."""
+def test_fp8_attention_headline_all_rows_of_sampled_heads(fa, causal):
+    """FP8 workload: B=16, H=16, N=8192, d=128 with outliers; every row of four seeded
+    heads against the oracle on the dequantised inputs (O and LSE) and, reported, on
+    the unquantised inputs."""
     heads = sampled_heads(16, 16)
-    rows = sampled_rows(8192, 96)
-    e = _fp8_case(fa, 16, 16, 8192, 128, causal, 0, seed=0, heads=heads, rows=rows)
-    print("fp8 headline errors", e)
+    e = _fp8_case(fa, 16, 16, 8192, 128, causal, 0, seed=0, heads=heads, rows=list(range(8192)))
+    print(f"fp8 headline causal={causal}:", e)
+    assert e["rows_checked"] == 4 * 8192
     assert e["vs_deq"] <= FP8_REL_RMSE_DEQ, e
     assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_REL_RMSE_DEQ, e
+    assert e["lse_bound_ratio"] <= 1.0, e
