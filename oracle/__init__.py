@@ -26,6 +26,9 @@ Functions and the passage each follows:
                              (fmt="e4m3", scale = amax/448), E5M2 (fmt="e5m2",
                              scale = amax/57344), or E4M3 with a power-of-two scale per
                              block (fmt="e4m3_pow2": the smallest 2^k >= amax/448)
+  fp8_block_rows             head-dim-aware scaling ([WGC] §3 头维度感知量化: the scaling
+                             is tuned separately for head dims 64 and 128 so that small head
+                             dims lose no precision): rows per scale block of Q, K and V
   dequantize                 x ~= x8 * scale for the block, the inverse map
   hadamard_rotate_f32        incoherent processing before quantisation ([JJ] §1
                              item 3, 块量化和无相关处理): orthonormal Walsh-Hadamard
@@ -385,6 +388,22 @@ def quantize_fp8_hadamard(x, block: int = 128):
     """Incoherent processing then per-block quantisation: quantize_fp8_blockwise of
     hadamard_rotate_f32(x).  Dequantised values approximate x @ H_d / sqrt(d)."""
     return quantize_fp8_blockwise(hadamard_rotate_f32(x), block)
+
+
+def fp8_block_rows(d: int, operand: str) -> int:
+    """Rows per FP8 scale block under head-dim-aware scaling.
+
+    [WGC] §3 FP8 量化与精度保持 says the scaling strategy is tuned separately for head
+    dims 64 and 128 so that small head dims do not lose precision, and gives no rule.
+    Reading: Q and K, whose products with each other run over the d entries of a row,
+    are scaled per block of min(d, 128) rows -- a d x d block at d = 64, the 128-row
+    block at d >= 128 (the FP8 workload's block); V, whose error in O averages over keys
+    rather than over d, keeps 128-row blocks at every d."""
+    if operand not in ("q", "k", "v"):
+        raise ValueError("operand must be 'q', 'k' or 'v'")
+    if d < 1:
+        raise ValueError("head dim must be positive")
+    return 128 if operand == "v" else min(int(d), 128)
 
 
 def dequantize(x8, scales, block: int = 128, fmt: str = "e4m3") -> np.ndarray:
