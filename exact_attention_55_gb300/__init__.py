@@ -348,8 +348,11 @@ def attn_decode_bf16_paged(q, k_cache, v_cache, page_table, seq_lens, scale: flo
 def attn_decode_bf16_paged_noalloc(q, k_cache, v_cache, page_table, seq_lens,
                                    scale: float | None = None, num_splits: int = 0, o=None,
                                    lse=None, stream=None):
-    """attn_decode_bf16_paged with the split partials in the library's own device
-    scratch (no workspace); calls on one device must be ordered."""
+    """attn_decode_bf16_paged for callers that cannot allocate device memory when they
+    decode: the split partials go to the library's own 16 MiB device scratch (no
+    workspace).  Calls on one device must be ordered (they share the scratch); a
+    forced num_splits whose partials exceed 16 MiB raises AttnError.  This wrapper
+    allocates o and lse when they are not given; pass them to allocate nothing."""
     B, H, nq, d, num_pages, page_size, max_pages, scale, o, lse = _decode_args(
         q, k_cache, v_cache, page_table, seq_lens, scale, o, lse)
     st = load_library().attn_decode_bf16_paged_noalloc(

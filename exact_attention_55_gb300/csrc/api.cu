@@ -26,8 +26,14 @@ cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count
 // One status word per device: kernels write kStatusTimeout here when they give up.
 __device__ int g_device_status;
 
-// Device-wide scratch for attn_decode_bf16_paged_noalloc: the split partials of a
-// decoding step live here instead of in a caller-provided workspace.  16 MB.
+// Device-wide scratch for attn_decode_bf16_paged_noalloc, the entry point for callers
+// that cannot allocate device memory when they decode: the split partials of a
+// decoding step live here instead of in a caller-provided workspace.  16 MiB, held
+// by every device that loads the library until the process exits.  Host code never
+// passes the symbol itself to a kernel (on the host it names a host-side stand-in);
+// device_info() looks up its device address once per device and caches it.  Every
+// split writes all of its partials before the merge reads them, so nothing here has
+// to start at zero; calls that overlap on the GPU race on it.
 constexpr size_t kDecodeScratchFloats = size_t(1) << 22;
 static __device__ __align__(256) float g_decode_scratch[kDecodeScratchFloats];
 

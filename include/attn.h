@@ -172,12 +172,27 @@ attn_status_t attn_decode_bf16_paged(const void* q, const void* k_cache, const v
 /*
  * attn_decode_bf16_paged_noalloc -- attn_decode_bf16_paged without a caller workspace.
  *
- * The split partials go to one 16 MB scratch array of the library on each device
- * (a file-scope static device array), so the call needs no memory from the caller.
- * With num_splits = 0 the plan shrinks to what the scratch holds; num_splits > 0
- * that does not fit is ATTN_ERR_INVALID_ARG.  The scratch is shared: calls through
- * this entry point on one device must be ordered (one stream, or streams the caller
- * synchronises); attn_decode_bf16_paged with a workspace per stream has no such rule.
+ * The pages have no counterpart to this entry point: it exists for callers that
+ * cannot allocate device memory when they decode.  Examples are an inference engine
+ * that divided the GPU's memory among its parts at start-up and hands a kernel only
+ * the tensors it computes on, and a latency-bound decoding loop in which cudaMalloc
+ * would synchronise the device and stall the other streams.  Such a caller passes
+ * only its inputs and outputs; the split partials go to a 16 MiB array
+ * (4,194,304 floats, a file-scope static device array of the library) that every
+ * device which loads the library holds until the process exits.  The entry point
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *   Set-up: the first call of any entry point of this library on a device looks up
+ *   that array's device address (cudaGetSymbolAddress, with the device current) and
+ *   caches it.  Make that first call before any stream capture begins.
+ *   Limit: the partials need B * H * splits * nq * (d + 1) * 4 bytes.  With
+ *   num_splits = 0 the plan shrinks to the splits that fit (one split needs no
+ *   partials); num_splits > 0 beyond 16 MiB returns ATTN_ERR_INVALID_ARG and
+ *   launches nothing.
+ *   Sharing: every call uses the same array and leaves its partials there.  Nothing
+ *   in it has to start at zero, because every split writes all of its partials
+ *   before the merge reads them.  Calls that overlap on the GPU race on the array:
+ *   issue calls on one device on one stream, or order the streams yourself.
+ *   attn_decode_bf16_paged with a workspace per stream has no such rule.
  */
 attn_status_t attn_decode_bf16_paged_noalloc(const void* q, const void* k_cache,
                                              const void* v_cache, const int* page_table,

@@ -78,26 +78,3 @@ def test_sequence_shorter_than_queries(fa):
     k0, v0 = kc[page, 0, 0].double(), vc[page, 0, 0].double()
     assert (o[0, 0, 2].double() - v0).abs().max() <= 1e-2      # one key: its value
     assert abs(float(lse[0, 0, 2]) - 0.2 * float((q[0, 0, 2].double() * k0).sum())) <= 1e-3
-
-
-def test_noalloc_entry_matches_workspace_entry(fa):
-    """The no-alloc entry point (library scratch) gives the workspace entry's result
-    bit for bit for the same split plan."""
-    for lens, H, nq, d, ps, splits in (([8192] * 16, 16, 1, 128, 64, 0),
-                                       ([2, 5000, 129, 3000], 4, 3, 64, 32, 5)):
-        q, kc, vc, pt, sl = (t.cuda() for t in make_paged_cache(lens, H, nq, d, ps, seed=84))
-        o1, l1 = fa.attn_decode_bf16_paged(q, kc, vc, pt, sl, num_splits=splits)
-        o2, l2 = fa.attn_decode_bf16_paged_noalloc(q, kc, vc, pt, sl, num_splits=splits)
-        torch.cuda.synchronize()
-        assert fa.attn_get_device_status() == fa.ATTN_OK
-        assert torch.equal(o1, o2) and torch.equal(l1, l2)
-
-
-def test_noalloc_rejects_a_forced_plan_larger_than_its_scratch(fa):
-    B, H, nq, d = 64, 32, 8, 256                # 8 splits need 134 MB > 16 MB of scratch
-    q = torch.zeros((B, H, nq, d), dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros((8, H, 16, d), dtype=torch.bfloat16, device="cuda")
-    pt = torch.zeros((B, 8), dtype=torch.int32, device="cuda")
-    sl = torch.full((B,), 100, dtype=torch.int32, device="cuda")
-    with pytest.raises(fa.AttnError):
-        fa.attn_decode_bf16_paged_noalloc(q, kc, kc, pt, sl, num_splits=8)
