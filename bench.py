@@ -499,6 +499,25 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
         "bar": 4e-2, **bars,
         "against": "attn_fwd_bf16 on the same (unquantised) bf16 inputs, all 256 heads"}
     del o_fp8, o_ref
+    # FP8 at head dim 64 with head-dim-aware scaling (Q, K per 64-row block, V per 128):
+    # the FP8 workload's distribution at B16 H16 N8192 d64
+    q6, k6, v6 = make_qkv(B, H, N, 64, seed=0, outliers=True)
+    q6, k6, v6 = q6.to(dev), k6.to(dev), v6.to(dev)
+    qkb = fa.attn_fp8_qk_block_rows(64)
+    (q68, sq6), (k68, sk6) = (fa.attn_quantize_fp8_blockwise(t, block=qkb) for t in (q6, k6))
+    v68, sv6 = fa.attn_quantize_fp8_blockwise(v6, block=128)
+    o6 = torch.empty_like(q6)
+    l6 = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        def fp8_d64_step():
+            fa.attn_fwd_fp8_blocks(q68, k68, v68, sq6, sk6, sv6, qk_block=qkb, scale=0.125,
+                                   causal=causal, o=o6, lse=l6, stream=stream)
+        ms, per = time_steps(fp8_d64_step, reps, 3, stream)
+        t = flops(B, H, N, 64, causal=causal) / (statistics.mean(per) * 1e-3) / 1e12
+        out["fp8_d64_causal" if causal else "fp8_d64"] = {
+            "tflops": t, "ms": statistics.mean(per), "frac_of_peak": t / peak8,
+            "shape": "B16 H16 N8192 d64", "qk_block_rows": qkb, "v_block_rows": 128}
+    del q6, k6, v6, q68, k68, v68, sq6, sk6, sv6, o6, l6
     # mixed FP8 formats: Q and K quantised to E5M2 (amax / 57344), V kept in E4M3
     qe, sqe = fa.attn_quantize_fp8_blockwise_fmt(q2d, "e5m2")
     ke, ske = fa.attn_quantize_fp8_blockwise_fmt(k2d, "e5m2")

@@ -31,10 +31,12 @@ __all__ = [
     "attn_fwd_bf16_varlen", "attn_decode_bf16_paged", "attn_decode_bf16_paged_noalloc",
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
-    "attn_quantize_fp8_blockwise_fmt", "attn_fwd_fp8_fmt", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
+    "attn_quantize_fp8_blockwise_fmt", "attn_fwd_fp8_fmt", "attn_fwd_fp8_blocks",
+    "attn_fp8_qk_block_rows", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
     "ATTN_FP8_E4M3_POW2",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
-    "EXPORTED_SYMBOLS",
+    "attn_selftest_fwd_withheld_load", "attn_selftest_quant_withheld_load",
+    "attn_selftest_bwd_withheld_load", "attn_selftest_fp8_convert", "EXPORTED_SYMBOLS",
 ]
 
 ATTN_OK = 0
@@ -58,8 +60,11 @@ EXPORTED_SYMBOLS = (
     "attn_decode_bf16_paged_noalloc", "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_blockwise_fmt",
     "attn_quantize_fp8_hadamard",
-    "attn_fwd_fp8", "attn_fwd_fp8_fmt", "attn_status_string", "attn_get_device_status",
-    "attn_selftest_wait_timeout",
+    "attn_fwd_fp8", "attn_fwd_fp8_fmt", "attn_fwd_fp8_blocks", "attn_fp8_qk_block_rows",
+    "attn_status_string", "attn_get_device_status",
+    "attn_selftest_wait_timeout", "attn_selftest_fwd_withheld_load",
+    "attn_selftest_quant_withheld_load", "attn_selftest_bwd_withheld_load",
+    "attn_selftest_fp8_convert",
 )
 
 _lock = threading.Lock()
@@ -118,12 +123,27 @@ def load_library(path: str | None = None):
         lib.attn_quantize_fp8_blockwise_fmt.restype = i
         lib.attn_fwd_fp8_fmt.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, i, vp]
         lib.attn_fwd_fp8_fmt.restype = i
+        lib.attn_fwd_fp8_blocks.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i,
+                                            i, i, vp]
+        lib.attn_fwd_fp8_blocks.restype = i
+        lib.attn_fp8_qk_block_rows.argtypes = [i]
+        lib.attn_fp8_qk_block_rows.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i
         lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
         lib.attn_selftest_wait_timeout.restype = i
+        u64 = ctypes.c_ulonglong
+        lib.attn_selftest_fwd_withheld_load.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, u64, vp]
+        lib.attn_selftest_fwd_withheld_load.restype = i
+        lib.attn_selftest_quant_withheld_load.argtypes = [vp, vp, vp, i, i, i, i, i, u64, vp]
+        lib.attn_selftest_quant_withheld_load.restype = i
+        lib.attn_selftest_bwd_withheld_load.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                        ctypes.c_size_t, i, i, i, i, i, i, u64, vp]
+        lib.attn_selftest_bwd_withheld_load.restype = i
+        lib.attn_selftest_fp8_convert.argtypes = [ctypes.c_uint, ctypes.c_size_t, i, vp, vp]
+        lib.attn_selftest_fp8_convert.restype = i
         _lib = lib
         return lib
 
@@ -380,7 +400,8 @@ def _quant_outputs(x, block, x8, scales):
 
 
 def attn_quantize_fp8_blockwise(x, block: int = 128, x8=None, scales=None, stream=None):
-    """Per-(head, 128-row block) E4M3 quantisation; returns (x8 uint8 codes, fp32 scales)."""
+    """Per-(head, block of `block` rows) E4M3 quantisation, block = 128 or 64 (the
+    head-dim-aware Q / K block at d = 64); returns (x8 uint8 codes, fp32 scales)."""
     _check_bhnd("x", x, torch.bfloat16)
     B, H, N, d = x.shape
     x8, scales = _quant_outputs(x, block, x8, scales)
@@ -441,8 +462,27 @@ def attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, qk_fmt, v_fmt=
                     descale_q, descale_k, descale_v, scale, causal, window, o, lse, stream)
 
 
+def attn_fwd_fp8_blocks(q8, k8, v8, descale_q, descale_k, descale_v, qk_block: int | None = None,
+                        qk_fmt="e4m3", v_fmt="e4m3", scale: float | None = None,
+                        causal: bool = False, window: int = 0, o=None, lse=None, stream=None):
+    """attn_fwd_fp8_fmt with Q and K scaled per block of qk_block rows (64 or 128; V per 128
+    rows).  The default is the head-dim-aware block, attn_fp8_qk_block_rows(d): 64 rows at
+    d = 64, 128 above.  Quantise Q and K with attn_quantize_fp8_blockwise(x, block=qk_block)."""
+    d = q8.shape[-1]
+    if qk_block is None:
+        qk_block = attn_fp8_qk_block_rows(d)
+    return _fwd_fp8("attn_fwd_fp8_blocks", (_fp8_format(qk_fmt), _fp8_format(v_fmt), int(qk_block)),
+                    q8, k8, v8, descale_q, descale_k, descale_v, scale, causal, window, o, lse,
+                    stream, qk_block=int(qk_block))
+
+
+def attn_fp8_qk_block_rows(d: int) -> int:
+    """Rows per Q / K scale block under head-dim-aware scaling: min(d, 128)."""
+    return int(load_library().attn_fp8_qk_block_rows(int(d)))
+
+
 def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, causal, window,
-             o, lse, stream):
+             o, lse, stream, qk_block=128):
     views = []
     for n, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
@@ -461,8 +501,10 @@ def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, 
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
     _check_out(o, (B, H, N, d), torch.bfloat16, q8.device, "o")
     _check_out(lse, (B, H, N), torch.float32, q8.device, "lse")
-    for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
-        _check_out(t, (B, H, (N + 127) // 128), torch.float32, q8.device, n)
+    nqk = (N + qk_block - 1) // qk_block
+    for n, t, nb in (("descale_q", descale_q, nqk), ("descale_k", descale_k, nqk),
+                     ("descale_v", descale_v, (N + 127) // 128)):
+        _check_out(t, (B, H, nb), torch.float32, q8.device, n)
     args = [q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), descale_q.data_ptr(), descale_k.data_ptr(),
             descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
             int(bool(causal)), int(window)]
@@ -482,3 +524,55 @@ def attn_selftest_wait_timeout(timeout_ns: int = 50_000_000, stream=None) -> Non
     """Run the bounded-wait self-test kernel (it records ATTN_ERR_TIMEOUT on purpose)."""
     st = load_library().attn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream))
     _raise_if(st, "attn_selftest_wait_timeout")
+
+
+def attn_selftest_fwd_withheld_load(q, k, v, o, lse, causal: bool = False, withheld: int = 2,
+                                    timeout_ns: int = 20_000_000, stream=None) -> None:
+    """Run the bf16 forward kernel with K/V load `withheld` of every CTA never issued and
+    every wait bounded by timeout_ns: the kernel aborts and records ATTN_ERR_TIMEOUT
+    (read it with attn_get_device_status); o and lse are left unspecified."""
+    B, H, N, d = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_bhnd(n, t, torch.bfloat16)
+    st = load_library().attn_selftest_fwd_withheld_load(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+        int(bool(causal)), int(withheld), int(timeout_ns), _stream_handle(stream))
+    _raise_if(st, "attn_selftest_fwd_withheld_load")
+
+
+def attn_selftest_quant_withheld_load(x, x8, scales, withheld: int = 1,
+                                      timeout_ns: int = 20_000_000, stream=None) -> None:
+    """Run the E4M3 block quantiser with block load `withheld` of every CTA never issued
+    and every wait bounded by timeout_ns (it records ATTN_ERR_TIMEOUT)."""
+    B, H, N, d = x.shape
+    _check_bhnd("x", x, torch.bfloat16)
+    st = load_library().attn_selftest_quant_withheld_load(
+        x.data_ptr(), x8.data_ptr(), scales.data_ptr(), B, H, N, d, int(withheld),
+        int(timeout_ns), _stream_handle(stream))
+    _raise_if(st, "attn_selftest_quant_withheld_load")
+
+
+def attn_selftest_bwd_withheld_load(q, k, v, o, dout, lse, dq, dk, dv, workspace,
+                                    causal: bool = False, withheld: int = 2,
+                                    timeout_ns: int = 20_000_000, stream=None) -> None:
+    """Run the backward kernels with ring load `withheld` of every CTA never issued and
+    every wait bounded by timeout_ns (they record ATTN_ERR_TIMEOUT)."""
+    B, H, N, d = q.shape
+    st = load_library().attn_selftest_bwd_withheld_load(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), B, H, N, d, int(bool(causal)),
+        int(withheld), int(timeout_ns), _stream_handle(stream))
+    _raise_if(st, "attn_selftest_bwd_withheld_load")
+
+
+def attn_selftest_fp8_convert(first: int, count: int, fmt="e4m3", codes=None, stream=None):
+    """Device FP8 codes (the quantisers' conversion) of the fp32 bit patterns first ..
+    first + count - 1; returns a uint8 CUDA tensor of count codes."""
+    if codes is None:
+        codes = torch.empty(int(count), dtype=torch.uint8, device="cuda")
+    st = load_library().attn_selftest_fp8_convert(int(first), int(count), _fp8_format(fmt),
+                                                  codes.data_ptr(), _stream_handle(stream))
+    _raise_if(st, "attn_selftest_fp8_convert")
+    return codes
+

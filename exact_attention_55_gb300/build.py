@@ -32,6 +32,7 @@ UNITS = [
     ("fwd_bf16_d64", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=64", "-DGB300_ATTN_F8=0"]),
     ("fwd_bf16_d128", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=128", "-DGB300_ATTN_F8=0"]),
     ("fwd_bf16_d256", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=256", "-DGB300_ATTN_F8=0"]),
+    ("fwd_fp8_d64", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=64", "-DGB300_ATTN_F8=1"]),
     ("fwd_fp8_d128", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=128", "-DGB300_ATTN_F8=1"]),
     ("fwd_fp8_d256", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=256", "-DGB300_ATTN_F8=1"]),
 ]

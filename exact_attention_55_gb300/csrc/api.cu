@@ -20,6 +20,8 @@
 namespace gb300 {
 
 cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t stream);
+cudaError_t launch_fp8_convert(uint32_t first, size_t count, int fmt, void* codes, int sm_count,
+                               cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count, cudaStream_t stream);
 
@@ -103,14 +105,16 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // 3-D map over a [BH, N, d] tensor: dims (d, N, BH) innermost first, 128-byte
 // swizzled boxes of (128 bytes of d) x box_rows x 1.  Rows past N read as zero.
 bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int d,
-               int N, int BH, int box_rows)
+               int N, int BH, int box_rows, int swz = 128)
 {
+    // swz: swizzle span in bytes, 128 or (rows of exactly 64 bytes) 64
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)N * d * elem_bytes};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows, 1};
+    cuuint32_t box[3] = {(cuuint32_t)(swz / elem_bytes), (cuuint32_t)box_rows, 1};
     cuuint32_t estride[3] = {1, 1, 1};
     CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estride,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -173,7 +177,9 @@ attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* 
 template <int D, bool F8>
 attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                       const float* dq, const float* dk, const float* dv, int BH, int N, float scale,
-                      int causal, int window, cudaStream_t stream, int qk_fmt = 0, int v_pow2 = 0)
+                      int causal, int window, cudaStream_t stream, int qk_fmt = 0, int v_pow2 = 0,
+                      unsigned long long timeout_ns = kWaitTimeoutNs, int withhold_kv = 0,
+                      int qk_block = 128)
 {
     using C = FwdCfg<D, F8>;
     DeviceInfo* dev = nullptr;
@@ -182,9 +188,9 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     const CUtensorMapDataType dt =
         F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     alignas(64) CUtensorMap mq, mk, mv;
-    if (!encode_3d(&mq, q, dt, C::EB, D, N, BH, C::BM) ||
-        !encode_3d(&mk, k, dt, C::EB, D, N, BH, C::BN) ||
-        !encode_3d(&mv, v, dt, C::EB, D, N, BH, C::BN))
+    if (!encode_3d(&mq, q, dt, C::EB, D, N, BH, C::BM, C::SWZ) ||
+        !encode_3d(&mk, k, dt, C::EB, D, N, BH, C::BN, C::SWZ) ||
+        !encode_3d(&mv, v, dt, C::EB, D, N, BH, C::BN, C::SWZ))
         return ATTN_ERR_CUDA;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -203,9 +209,11 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.causal = causal ? 1 : 0;
     p.window = window > 0 ? window : 0;
     p.c_log2 = (float)((double)scale * 1.4426950408889634);
-    p.timeout_ns = kWaitTimeoutNs;
+    p.timeout_ns = timeout_ns;
+    p.withhold_kv = withhold_kv;
     p.qk_fmt = qk_fmt;
     p.v_pow2 = v_pow2;
+    p.qk_shift = qk_block == 64 ? 6 : 7;
     if (launch_attn_fwd<D, F8>(mq, mk, mv, p, dev->sm_count, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -298,14 +306,45 @@ extern "C" attn_status_t attn_fwd_bf16_varlen(const void* q, const void* k, cons
     }
 }
 
+static attn_status_t fwd_fp8(const void* q8, const void* k8, const void* v8,
+                             const float* descale_q, const float* descale_k,
+                             const float* descale_v, void* o, float* lse, int B, int H, int N,
+                             int d, float scale, int causal, int window, int qk_format,
+                             int v_format, int qk_block, void* stream)
+{
+    if (!q8 || !k8 || !v8 || !descale_q || !descale_k || !descale_v || !o || !lse)
+        return ATTN_ERR_INVALID_ARG;
+    if (qk_format != ATTN_FP8_E4M3 && qk_format != ATTN_FP8_E5M2 && qk_format != ATTN_FP8_E4M3_POW2)
+        return ATTN_ERR_INVALID_ARG;
+    if (v_format != ATTN_FP8_E4M3 && v_format != ATTN_FP8_E4M3_POW2) return ATTN_ERR_INVALID_ARG;
+    if (qk_block != 64 && qk_block != 128) return ATTN_ERR_UNSUPPORTED;
+    const int qk_fmt = qk_format == ATTN_FP8_E5M2 ? 1 : 0;   // the codes' type in the QK^T MMA
+    const int v_pow2 = v_format == ATTN_FP8_E4M3_POW2 ? 1 : 0;
+    long long BH = 0;
+    attn_status_t st = check_common(B, H, N, scale, &BH);
+    if (st != ATTN_OK) return st;
+    if ((d != 64 && d != 128 && d != 256) || N % 128 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(descale_q, 4) || !aligned(descale_k, 4) ||
+        !aligned(descale_v, 4))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned long long t = kWaitTimeoutNs;
+    switch (d) {
+        case 64: return run_fwd<64, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2, t, 0, qk_block);
+        case 128: return run_fwd<128, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2, t, 0, qk_block);
+        default: return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2, t, 0, qk_block);
+    }
+}
+
 extern "C" attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
                                       const float* descale_q, const float* descale_k,
                                       const float* descale_v, void* o, float* lse, int B, int H,
                                       int N, int d, float scale, int causal, int window,
                                       void* stream)
 {
-    return attn_fwd_fp8_fmt(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale,
-                            causal, window, ATTN_FP8_E4M3, ATTN_FP8_E4M3, stream);
+    return fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
+                   window, ATTN_FP8_E4M3, ATTN_FP8_E4M3, 128, stream);
 }
 
 extern "C" attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const void* v8,
@@ -314,45 +353,47 @@ extern "C" attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const 
                                           int N, int d, float scale, int causal, int window,
                                           int qk_format, int v_format, void* stream)
 {
-    if (!q8 || !k8 || !v8 || !descale_q || !descale_k || !descale_v || !o || !lse)
-        return ATTN_ERR_INVALID_ARG;
-    if (qk_format != ATTN_FP8_E4M3 && qk_format != ATTN_FP8_E5M2 && qk_format != ATTN_FP8_E4M3_POW2)
-        return ATTN_ERR_INVALID_ARG;
-    if (v_format != ATTN_FP8_E4M3 && v_format != ATTN_FP8_E4M3_POW2) return ATTN_ERR_INVALID_ARG;
-    const int qk_fmt = qk_format == ATTN_FP8_E5M2 ? 1 : 0;   // the codes' type in the QK^T MMA
-    const int v_pow2 = v_format == ATTN_FP8_E4M3_POW2 ? 1 : 0;
-    long long BH = 0;
-    attn_status_t st = check_common(B, H, N, scale, &BH);
-    if (st != ATTN_OK) return st;
-    if ((d != 128 && d != 256) || N % 128 != 0) return ATTN_ERR_UNSUPPORTED;
-    if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(v8, 16) || !aligned(o, 16) ||
-        !aligned(lse, 4) || !aligned(descale_q, 4) || !aligned(descale_k, 4) ||
-        !aligned(descale_v, 4))
-        return ATTN_ERR_MISALIGNED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d == 128)
-        return run_fwd<128, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2);
-    return run_fwd<256, true>(q8, k8, v8, o, lse, descale_q, descale_k, descale_v, (int)BH, N, scale, causal, window, s, qk_fmt, v_pow2);
+    return fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
+                   window, qk_format, v_format, 128, stream);
+}
+
+extern "C" attn_status_t attn_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8,
+                                             const float* descale_q, const float* descale_k,
+                                             const float* descale_v, void* o, float* lse, int B,
+                                             int H, int N, int d, float scale, int causal,
+                                             int window, int qk_format, int v_format,
+                                             int qk_block, void* stream)
+{
+    return fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
+                   window, qk_format, v_format, qk_block, stream);
+}
+
+extern "C" int attn_fp8_qk_block_rows(int d)
+{
+    if (d < 1) return 0;
+    return d < 128 ? d : 128;
 }
 
 static attn_status_t quantize(const void* x, void* x8, float* scales, int B, int H, int N, int d,
-                              int block, bool rotate, void* stream, int fmt = ATTN_FP8_E4M3)
+                              int block, bool rotate, void* stream, int fmt = ATTN_FP8_E4M3,
+                              unsigned long long timeout_ns = kWaitTimeoutNs, int withhold = 0)
 {
     if (!x || !x8 || !scales) return ATTN_ERR_INVALID_ARG;
     if (fmt != ATTN_FP8_E4M3 && fmt != ATTN_FP8_E5M2 && fmt != ATTN_FP8_E4M3_POW2)
         return ATTN_ERR_INVALID_ARG;
     if (rotate && fmt != ATTN_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
-    if (block != 128 || d % 16 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
+    if ((block != 64 && block != 128) || d % 16 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
     if (rotate && d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
     if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scales, 4)) return ATTN_ERR_MISALIGNED;
     const long long BH = (long long)B * H;
-    const long long nblk = (N + 127) / 128;
+    const long long nblk = (N + block - 1) / block;
     if (BH * nblk > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     DeviceInfo* dev = nullptr;
     attn_status_t st = device_info(&dev);
     if (st != ATTN_OK) return st;
     QuantParams p;
+    std::memset(&p, 0, sizeof(p));
     p.x = x;
     p.x8 = static_cast<uint8_t*>(x8);
     p.scales = scales;
@@ -361,9 +402,12 @@ static attn_status_t quantize(const void* x, void* x8, float* scales, int B, int
     p.N = N;
     p.d = d;
     p.nblk = (int)nblk;
+    p.rows = block;
     p.rotate = rotate ? 1 : 0;
     p.rot_c = (float)(1.0 / sqrt((double)d));
     p.fmt = fmt;
+    p.timeout_ns = timeout_ns;
+    p.withhold = withhold;
     if (launch_quant_fp8(p, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -425,6 +469,82 @@ extern "C" attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_n
     if (st != ATTN_OK) return st;
     wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, timeout_ns);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+static attn_status_t bwd_batched(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                 void* workspace, size_t workspace_bytes, int B, int H, int N,
+                                 int d, float scale, int causal, int window, void* stream,
+                                 unsigned long long timeout_ns, int withhold_ring);
+
+extern "C" attn_status_t attn_selftest_fp8_convert(unsigned int first, size_t count, int format,
+                                                   void* codes, void* stream)
+{
+    if (!codes || count == 0 || count % 8 != 0) return ATTN_ERR_INVALID_ARG;
+    if (format != ATTN_FP8_E4M3 && format != ATTN_FP8_E5M2) return ATTN_ERR_INVALID_ARG;
+    if ((unsigned long long)first + count > (1ull << 32)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(codes, 16)) return ATTN_ERR_MISALIGNED;
+    DeviceInfo* dev = nullptr;
+    attn_status_t st = device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (launch_fp8_convert(first, count, format == ATTN_FP8_E5M2 ? 1 : 0, codes, dev->sm_count,
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+// The real kernels with one load withheld (the test hooks in their parameters) and a
+// short per-wait limit: the waits on the missing load run out, the CTA aborts through
+// its normal failure path and the status word reads ATTN_ERR_TIMEOUT.
+static bool selftest_args_ok(int withheld, unsigned long long timeout_ns)
+{
+    return withheld >= 0 && withheld < 0x7ffffffe && timeout_ns > 0 && timeout_ns <= 2000000000ull;
+}
+
+extern "C" attn_status_t attn_selftest_fwd_withheld_load(const void* q, const void* k,
+                                                        const void* v, void* o, float* lse, int B,
+                                                        int H, int N, int d, int causal,
+                                                        int withheld,
+                                                        unsigned long long timeout_ns,
+                                                        void* stream)
+{
+    if (!selftest_args_ok(withheld, timeout_ns)) return ATTN_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    long long BH = 0;
+    attn_status_t st = check_common(B, H, N, 1.0f, &BH);
+    if (st != ATTN_OK) return st;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float scale = 1.0f / sqrtf((float)d);
+    switch (d) {
+        case 64: return run_fwd<64, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, 0, s, 0, 0, timeout_ns, withheld + 1);
+        case 128: return run_fwd<128, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, 0, s, 0, 0, timeout_ns, withheld + 1);
+        case 256: return run_fwd<256, false>(q, k, v, o, lse, nullptr, nullptr, nullptr, (int)BH, N, scale, causal, 0, s, 0, 0, timeout_ns, withheld + 1);
+        default: return ATTN_ERR_UNSUPPORTED;
+    }
+}
+
+extern "C" attn_status_t attn_selftest_quant_withheld_load(const void* x, void* x8, float* scales,
+                                                          int B, int H, int N, int d,
+                                                          int withheld,
+                                                          unsigned long long timeout_ns,
+                                                          void* stream)
+{
+    if (!selftest_args_ok(withheld, timeout_ns)) return ATTN_ERR_INVALID_ARG;
+    return quantize(x, x8, scales, B, H, N, d, 128, false, stream, ATTN_FP8_E4M3, timeout_ns,
+                    withheld + 1);
+}
+
+extern "C" attn_status_t attn_selftest_bwd_withheld_load(
+    const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
+    int d, int causal, int withheld, unsigned long long timeout_ns, void* stream)
+{
+    if (!selftest_args_ok(withheld, timeout_ns)) return ATTN_ERR_INVALID_ARG;
+    return bwd_batched(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                       1.0f / sqrtf((float)d), causal, 0, stream, timeout_ns, withheld + 1);
 }
 
 extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int page_size,
@@ -596,11 +716,11 @@ extern "C" attn_status_t attn_bwd_bf16_varlen(const void* q, const void* k, cons
     return ATTN_OK;
 }
 
-extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
-                                      const void* dout, const float* lse, void* dq, void* dk,
-                                      void* dv, void* workspace, size_t workspace_bytes, int B,
-                                      int H, int N, int d, float scale, int causal, int window,
-                                      void* stream)
+static attn_status_t bwd_batched(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                 void* workspace, size_t workspace_bytes, int B, int H, int N,
+                                 int d, float scale, int causal, int window, void* stream,
+                                 unsigned long long timeout_ns, int withhold_ring)
 {
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
         return ATTN_ERR_INVALID_ARG;
@@ -645,8 +765,19 @@ extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void*
     p.window = window > 0 ? window : 0;
     p.c_log2 = (float)((double)scale * 1.4426950408889634);
     p.scale = scale;
-    p.timeout_ns = kWaitTimeoutNs;
+    p.timeout_ns = timeout_ns;
+    p.withhold_ring = withhold_ring;
     if (launch_bwd(maps, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
+}
+
+extern "C" attn_status_t attn_bwd_bf16(const void* q, const void* k, const void* v, const void* o,
+                                      const void* dout, const float* lse, void* dq, void* dk,
+                                      void* dv, void* workspace, size_t workspace_bytes, int B,
+                                      int H, int N, int d, float scale, int causal, int window,
+                                      void* stream)
+{
+    return bwd_batched(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                       scale, causal, window, stream, kWaitTimeoutNs, 0);
 }

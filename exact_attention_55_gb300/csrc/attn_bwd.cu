@@ -43,6 +43,7 @@
 
 #include "attn_params.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace gb300 {
 
@@ -56,7 +57,9 @@ struct BwdCfg {
     static constexpr int RING_CB = BC * 128;       // one column block of a ring tile
     static constexpr int RING_BYTES = NCB * RING_CB;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = kDQ ? 512 : 512 + 4096;   // barriers (+ dK/dV: per-warp LSE / D)
+    // barriers (+ dK/dV: per-warp LSE / D at +512), then the packed-sequence schedule table
+    static constexpr int TAB_OFF = kDQ ? 256 : 512 + 4096;
+    static constexpr int BAR_BYTES = TAB_OFF + 1792;
     static constexpr int ALIGN_SLACK = 1024;
     // A ring slot holds one tile (dQ pass: V_j and K_j have different lifetimes) or a
     // step's two tiles under one barrier pair (dK/dV pass: Q_i and dO_i are used alike).
@@ -87,6 +90,7 @@ struct BwdCfg {
     static_assert(kDQ ? ACC_COL + D <= TMEM_COLS : ACC_COL + 2 * D <= TMEM_COLS, "TMEM budget");
     static_assert(NSLOT >= (kDQ ? 5 : 4), "ring too small");
     static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory");
+    static_assert(sizeof(SortTab) <= 1792, "schedule table");
 };
 
 struct alignas(16) BwdBars {
@@ -168,14 +172,25 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, const BwdUnit& u, 
 // the middle tile of an odd tile count appears once.  Packed sequences: pair slots are
 // laid out for the longest sequence and a shorter one skips the slots it does not have;
 // offsets are clamped to [0, T] so a unit never addresses a token outside the tensors.
+// With up to kSortMaxSeqs packed sequences the pairs are instead dealt longest sequence
+// first in snake order from the table each CTA sorts (sched.cuh).
 template <bool kPacked>
-__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u)
+__device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u, const SortTab* tab)
 {
     const int npair = (p.nt + 1) >> 1;
     const int pair = s >> 1;
-    const int sh = pair / npair;                 // batched: bh; packed: sequence * H + head
-    const int k = pair - sh * npair;
+    int sh = pair / npair;                       // batched: bh; packed: sequence * H + head
+    int k = pair - sh * npair;
     u.packed = kPacked;
+    if (kPacked && tab != nullptr) {
+        int seq, rem, a, b;
+        sorted_pair(tab, p.num_seqs, pair, seq, rem);
+        seq_span(p.cu_seqlens, seq, p.T, a, b);
+        const int np = (((b - a + 127) / 128) + 1) >> 1;   // > 0 for a sequence that holds pairs
+        const int h = rem / np;
+        k = rem - h * np;
+        sh = seq * p.H + h;
+    }
     if (!u.packed) {
         u.N = p.N;
         u.c1 = 0;
@@ -200,7 +215,11 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u)
     return !((s & 1) && k == nt - 1 - k);
 }
 
-__device__ __forceinline__ int bwd_next(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
+__device__ __forceinline__ int bwd_next(int s, const SortTab* tab)
+{
+    if (!(s & 1)) return s + 1;
+    return tab != nullptr ? snake_next_sub(s) : s + 2 * (int)gridDim.x - 1;
+}
 
 // True when every (query, key) pair of the block of queries [q0, q0 + nq) and keys
 // [k0, k0 + nk) lies inside the sequence and is allowed by the mask, so the step needs
@@ -257,7 +276,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
     BwdBars* bars = reinterpret_cast<BwdBars*>(ring + C::NSLOT * C::SLOT_BYTES);
     const volatile int* abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nsub = 2 * ((p.nt + 1) >> 1) * p.BH;   // sub-units (see bwd_unit)
+    int nsub = 2 * ((p.nt + 1) >> 1) * p.BH;         // sub-units (see bwd_unit)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->fix_full), 1);
@@ -286,6 +305,16 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // packed sequences: the sorted schedule (every thread takes part; same in all CTAs)
+    const SortTab* tab = nullptr;
+    if constexpr (kPacked) {
+        if (p.num_seqs <= kSortMaxSeqs) {
+            SortTab* t = reinterpret_cast<SortTab*>(reinterpret_cast<uint8_t*>(bars) + C::TAB_OFF);
+            build_sort_tab<128>(p.cu_seqlens, p.num_seqs, p.T, p.H, t);
+            tab = t;
+            nsub = 2 * t->total;
+        }
+    }
 
     if (warp == C::PRODUCER_WARP) {
         regs_decrease<C::REG_CONTROL>();
@@ -294,9 +323,9 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             const uint64_t pol_ring = l2_policy_evict_last();
             uint32_t rc = 0, uc = 0, armed = 0;
             bool ok = true;
-            for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+            for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su, tab)) {
                 BwdUnit un;
-                if (!bwd_unit<kPacked>(p, su, un)) continue;
+                if (!bwd_unit<kPacked>(p, su, un, tab)) continue;
                 const int t = un.t;
                 int lo, hi;
                 bwd_steps(p, un, !kDQ, C::BC, lo, hi);
@@ -327,6 +356,11 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                                 ok = false;
                                 break;
                             }
+                            if (rc + 1 == (uint32_t)p.withhold_ring) {  // test hook: never arrives
+                                ++rc;
+                                if (!kDQ) break;    // the slot's second tile is not loaded either
+                                continue;
+                            }
                             mbar_arrive_expect_tx(rb, C::SLOT_BYTES);
                         }
                         const CUtensorMap* map = (which == 0) == kDQ ? &tmRingB : &tmRingA;
@@ -341,15 +375,18 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 }
                 ++uc;
             }
-            if (!ok) {
-                bwd_timeout(p, bars);
-                const uint32_t n = rc < C::NSLOT ? rc : C::NSLOT;
-                for (uint32_t k = rc - n; k < rc; ++k)
-                    mbar_wait(smem_u32(&bars->ring_full[k % C::NSLOT]), (k / C::NSLOT) & 1, nullptr,
-                              p.timeout_ns);
-                if (armed > 0)
-                    mbar_wait(smem_u32(&bars->fix_full), (armed - 1) & 1, nullptr, p.timeout_ns);
+            if (!ok) bwd_timeout(p, bars);
+            // Every copy this producer issued lands before shared memory is released (after
+            // an abort by another role they may still be in flight even when this loop
+            // ended normally); copies end on their own, hence the fixed cleanup bound.
+            const uint32_t n = rc < C::NSLOT ? rc : C::NSLOT;
+            for (uint32_t k = rc - n; k < rc; ++k) {
+                if (k + 1 == (uint32_t)p.withhold_ring) continue;  // never issued
+                mbar_wait(smem_u32(&bars->ring_full[k % C::NSLOT]), (k / C::NSLOT) & 1, nullptr,
+                          kCleanupTimeoutNs);
             }
+            if (armed > 0)
+                mbar_wait(smem_u32(&bars->fix_full), (armed - 1) & 1, nullptr, kCleanupTimeoutNs);
         }
     } else if (warp == C::MMA_WARP) {
       if constexpr (kDQ) {
@@ -397,9 +434,9 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 mma_ts_warp<false>(tmem + C::ACC_COL, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8,
                                    b0 + ((kk * 16 * 128) >> 4), idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
-        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su, tab)) {
             BwdUnit un;
-            if (!bwd_unit<kPacked>(p, su, un)) continue;
+            if (!bwd_unit<kPacked>(p, su, un, tab)) continue;
             int lo, hi;
             bwd_steps(p, un, false, C::BC, lo, hi);
             const uint32_t r0 = rc, h0 = hs;            // tiles: V_j at r0 + 2(j-lo), K_j next
@@ -454,7 +491,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         }
         if (!ok && lane == 0) bwd_timeout(p, bars);
         commit(&bars->drain);
-        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, kCleanupTimeoutNs);
         __syncwarp();
       } else {
         // ---------------------------------------------------------------- MMA, dK/dV pass
@@ -492,9 +529,9 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 mma_ts_warp<false>(tmem + acc_col, tmem + a_col + kk * 8, bmn + ((kk * 16 * 128) >> 4),
                                    idesc_acc, (kk > 0 || accumulate) ? 1u : 0u);
         };
-        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su, tab)) {
             BwdUnit un;
-            if (!bwd_unit<kPacked>(p, su, un)) continue;
+            if (!bwd_unit<kPacked>(p, su, un, tab)) continue;
             int lo, hi;
             bwd_steps(p, un, !kDQ, C::BC, lo, hi);
             if (!wait(&bars->fix_full, uc & 1)) break;
@@ -544,7 +581,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         }
         if (!ok && lane == 0) bwd_timeout(p, bars);
         commit(&bars->drain);
-        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, kCleanupTimeoutNs);
         __syncwarp();
       }
     } else if (warp < C::COMPUTE_WARPS) {
@@ -575,9 +612,9 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             l2v = make_float2(__ldg(p.lse + base + c0) * LOG2E, __ldg(p.lse + base + c1) * LOG2E);
             dv = make_float2(__ldg(p.delta + base + c0), __ldg(p.delta + base + c1));
         };
-        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su)) {
+        for (int su = 2 * (int)blockIdx.x; su < nsub && ok; su = bwd_next(su, tab)) {
             BwdUnit un;
-            if (!bwd_unit<kPacked>(p, su, un)) continue;
+            if (!bwd_unit<kPacked>(p, su, un, tab)) continue;
             const int t = un.t, NS = un.N;              // tile and sequence length
             int lo, hi;
             bwd_steps(p, un, !kDQ, C::BC, lo, hi);
@@ -796,6 +833,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             ++uc;
         }
         if (!ok) bwd_timeout(p, bars);
+        tmem_wait_st();  // an aborted step may have left a P or dS store in flight
     } else {
         regs_decrease<C::REG_CONTROL>();                // spare warps of the control warpgroup
     }

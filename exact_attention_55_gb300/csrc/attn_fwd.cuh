@@ -34,23 +34,30 @@
 
 #include "attn_params.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace gb300 {
 
-template <int D, bool F8>
+template <int D, bool F8, bool PK = false, bool Q64 = false>
 struct FwdCfg {
+    static constexpr bool PACKED = PK;                   // packed variable-length sequences
+    // fp8: Q and K scaled per 64-row block (two K descales per 128-key tile); otherwise 128
+    static constexpr bool QK64 = Q64;
     static constexpr int BM = 128;                       // query rows per Q tile (MMA M)
     static constexpr int NQ = (D <= 128) ? 2 : 1;        // Q tiles per work unit
     static constexpr int BN = (D == 256 && !F8) ? 64 : 128;  // keys per K/V tile
     static constexpr int EB = F8 ? 1 : 2;                // bytes per operand element
-    static constexpr int SWE = 128 / EB;                 // elements per 128-byte swizzle row
-    static constexpr int NCB = D / SWE;                  // 128-byte column blocks per row
-    static constexpr int CB_Q_BYTES = BM * 128;
-    static constexpr int CB_KV_BYTES = BN * 128;
+    // swizzle span: 128 bytes, or 64 when a whole row is 64 bytes (fp8, d = 64)
+    static constexpr int SWZ = D * EB < 128 ? D * EB : 128;
+    static constexpr int SWE = SWZ / EB;                 // elements per swizzle row
+    static constexpr int NCB = D / SWE;                  // swizzle-row column blocks per row
+    static constexpr int CB_Q_BYTES = BM * SWZ;
+    static constexpr int CB_KV_BYTES = BN * SWZ;
     static constexpr int Q_BYTES = NCB * CB_Q_BYTES;
     static constexpr int KV_BYTES = NCB * CB_KV_BYTES;
     static constexpr int SMEM_CAP = 227 * 1024;
-    static constexpr int BAR_BYTES = 1024;
+    // barriers (FwdBars, 256 bytes at most) followed by the packed-sequence schedule table
+    static constexpr int BAR_BYTES = 2048;
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int NSLOT_FIT = (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - NQ * Q_BYTES) / KV_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
@@ -79,7 +86,8 @@ struct FwdCfg {
     static constexpr int P8_SHIFT = 8;
 
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
-    static_assert(!F8 || D >= 128, "fp8 needs a full 128-byte row");
+    static_assert(SWZ == 128 || SWZ == 64, "swizzle span");
+    static_assert(!F8 || BN == 128, "fp8: one 128-row V scale block per key tile");
     static_assert(NSLOT >= 3, "ring too small");
     static_assert(O_COL0 + NQ * D <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM_BYTES <= SMEM_CAP, "shared memory budget");
@@ -100,6 +108,11 @@ struct alignas(8) FwdBars {
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// Packed sequences: the schedule table (sched.cuh) sits in the barrier block.
+constexpr int kSortTabOffset = 256;  // bytes into the barrier block
+static_assert(kSortTabOffset + sizeof(SortTab) <= 2048, "schedule table must fit the barrier block");
+static_assert(sizeof(FwdBars) <= kSortTabOffset, "barriers must end before the schedule table");
 
 struct Unit {
     int z;       // batched: flattened (batch, head); packed sequences: the head
@@ -124,22 +137,35 @@ struct Unit {
 // shorter one skips the slots it does not have; offsets are clamped to [0, T] so
 // a unit never addresses a token outside the tensors.
 template <class C>
-__device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w)
+__device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w, const SortTab* tab)
 {
     const int npair = (p.num_qblk + 1) >> 1;
     const int pair = s >> 1;
-    const int k = pair % npair;
+    int k = pair % npair;
     int nq = p.num_qblk;
-    if (p.cu_seqlens == nullptr) {
+    if constexpr (!C::PACKED) {
         w.z = pair / npair;
         w.y0 = 0;
         w.N = p.N;
+    } else if (tab != nullptr) {
+        // sorted packed sequences (sched.cuh)
+        int seq, rem, a, b;
+        sorted_pair(tab, p.num_seqs, pair, seq, rem);
+        seq_span(p.cu_seqlens, seq, p.T, a, b);
+        w.y0 = a;
+        w.N = b - a;
+        nq = (w.N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+        const int np = (nq + 1) >> 1;                 // > 0: empty sequences hold no pairs
+        w.z = rem / np;
+        k = rem - w.z * np;
     } else {
+        // more sequences than the table holds: round-robin over pair slots laid out
+        // for the longest sequence; a shorter one skips the slots it does not have
         const int sh = pair / npair;
         const int seq = sh / p.H;
         w.z = sh - seq * p.H;
-        const int a = min(max(__ldg(p.cu_seqlens + seq), 0), p.T);
-        const int b = min(max(__ldg(p.cu_seqlens + seq + 1), a), p.T);
+        int a, b;
+        seq_span(p.cu_seqlens, seq, p.T, a, b);
         w.y0 = a;
         w.N = b - a;
         nq = (w.N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
@@ -159,6 +185,20 @@ __device__ __forceinline__ bool unit_of(int s, const FwdParams& p, Unit& w)
 }
 
 __device__ __forceinline__ int next_sub(int s) { return (s & 1) ? s + 2 * (int)gridDim.x - 1 : s + 1; }
+
+// The next sub-unit of this CTA: the second half of its pair, or the first half of its
+// pair in the next round -- round-robin, or snake order over the sorted table.
+__device__ __forceinline__ int next_sub(int s, const SortTab* tab)
+{
+    if (tab == nullptr || !(s & 1)) return next_sub(s);
+    return snake_next_sub(s);
+}
+
+// Sub-units [0, 2 * pairs) exist: pair slots of the layout, or the table's exact count.
+__device__ __forceinline__ int num_subs(const FwdParams& p, const SortTab* tab)
+{
+    return 2 * (tab != nullptr ? tab->total : p.num_units);
+}
 
 // Steps [L, R) of the unit's key-tile range that Q tile i needs: a key tile is
 // skipped for a Q tile when every (row, key) pair of it is masked (causal: all
@@ -190,12 +230,12 @@ __device__ __forceinline__ void raise_timeout(const FwdParams& p, FwdBars* bars)
     *reinterpret_cast<volatile int*>(&bars->abort_flag) = 1;
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool PK = false, bool QK64 = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p)
 {
-    using C = FwdCfg<D, F8>;
+    using C = FwdCfg<D, F8, PK, QK64>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -206,6 +246,16 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
+    // packed sequences: the sorted schedule (every thread takes part; same result in all CTAs)
+    const SortTab* tab = nullptr;
+    if constexpr (C::PACKED) {
+        if (p.num_seqs <= kSortMaxSeqs) {
+            SortTab* t = reinterpret_cast<SortTab*>(reinterpret_cast<uint8_t*>(bars) + kSortTabOffset);
+            build_sort_tab<C::NQ * C::BM>(p.cu_seqlens, p.num_seqs, p.T, p.H, t);
+            tab = t;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -246,9 +296,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             uint32_t ring = 0, uc = 0;
             uint32_t q_armed[2] = {0, 0};
             bool ok = true;
-            for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+            for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
                 Unit w;
-                if (!unit_of<C>(su, p, w)) continue;
+                if (!unit_of<C>(su, p, w, tab)) continue;
                 for (int i = 0; i < C::NQ && ok; ++i) {
                     const uint32_t fb = smem_u32(&bars->q_full[i]);
                     if (!mbar_wait(smem_u32(&bars->q_empty[i]), (uc & 1) ^ 1, abort_flag,
@@ -262,7 +312,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                     const int row = w.q0 + i * C::BM;
 #pragma unroll
                     for (int cb = 0; cb < C::NCB; ++cb) {
-                        if (p.cu_seqlens == nullptr)  // map (d, N, BH)
+                        if constexpr (!C::PACKED)  // map (d, N, BH)
                             tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE, row, w.z, pol_q);
                         else                          // map (d, H, T)
                             tma_load_3d(dst + cb * C::CB_Q_BYTES, &tmQ, fb, cb * C::SWE, w.z, w.y0 + row, pol_q);
@@ -279,13 +329,17 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                             ok = false;
                             break;
                         }
+                        if (ring + 1 == (uint32_t)p.withhold_kv) {  // test hook: never arrives
+                            ++ring;
+                            continue;
+                        }
                         const uint32_t fb = smem_u32(&bars->kv_full[slot]);
                         mbar_arrive_expect_tx(fb, C::KV_BYTES);
                         const uint32_t dst = smem_u32(kv_smem + slot * C::KV_BYTES);
                         const CUtensorMap* map = which == 0 ? &tmK : &tmV;
 #pragma unroll
                         for (int cb = 0; cb < C::NCB; ++cb) {
-                            if (p.cu_seqlens == nullptr)
+                            if constexpr (!C::PACKED)
                                 tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, c0, w.z, pol_kv);
                             else
                                 tma_load_3d(dst + cb * C::CB_KV_BYTES, map, fb, cb * C::SWE, w.z, w.y0 + c0, pol_kv);
@@ -295,19 +349,23 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 }
                 ++uc;
             }
-            if (!ok) {
-                raise_timeout(p, bars);
-                // Let every copy already issued land before shared memory is released:
-                // the latest arming of each ring slot and of each Q buffer.
-                const uint32_t armed = ring < C::NSLOT ? ring : C::NSLOT;
-                for (uint32_t k = ring - armed; k < ring; ++k)
-                    mbar_wait(smem_u32(&bars->kv_full[k % C::NSLOT]), (k / C::NSLOT) & 1,
-                              nullptr, p.timeout_ns);
-                for (int i = 0; i < C::NQ; ++i)
-                    if (q_armed[i] > 0)
-                        mbar_wait(smem_u32(&bars->q_full[i]), (q_armed[i] - 1) & 1, nullptr,
-                                  p.timeout_ns);
+            if (!ok) raise_timeout(p, bars);
+            // Every copy this producer issued lands before shared memory is released:
+            // wait for the latest arming of each ring slot and of each Q buffer.  On
+            // the normal path the consumers have waited for them too; after an abort
+            // by another role (which may come after this loop ended normally) they
+            // may still be in flight.  Copies end on their own, so the bound is the
+            // fixed cleanup one, not the per-wait limit.
+            const uint32_t armed = ring < C::NSLOT ? ring : C::NSLOT;
+            for (uint32_t k = ring - armed; k < ring; ++k) {
+                if (k + 1 == (uint32_t)p.withhold_kv) continue;  // never issued
+                mbar_wait(smem_u32(&bars->kv_full[k % C::NSLOT]), (k / C::NSLOT) & 1,
+                          nullptr, kCleanupTimeoutNs);
             }
+            for (int i = 0; i < C::NQ; ++i)
+                if (q_armed[i] > 0)
+                    mbar_wait(smem_u32(&bars->q_full[i]), (q_armed[i] - 1) & 1, nullptr,
+                              kCleanupTimeoutNs);
         }
     } else if (warp == C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
@@ -322,9 +380,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
         const uint32_t idesc_s = F8 ? idesc_f32acc(p.qk_fmt ? 1u : 0u, 0, C::BM, C::BN)
                                     : idesc_f32acc(fmt, 0, C::BM, C::BN);
         constexpr uint32_t idesc_o = idesc_f32acc(fmt, 1, C::BM, D);
-        const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_smem), 16, 1024);
-        const uint64_t k_desc0 = sdesc_sw128(smem_u32(kv_smem), 16, 1024);
-        const uint64_t v_desc0 = sdesc_sw128(smem_u32(kv_smem), C::CB_KV_BYTES, 1024);
+        const uint64_t q_desc0 = sdesc_sw<C::SWZ>(smem_u32(q_smem), 16, 8 * C::SWZ);
+        const uint64_t k_desc0 = sdesc_sw<C::SWZ>(smem_u32(kv_smem), 16, 8 * C::SWZ);
+        const uint64_t v_desc0 = sdesc_sw<C::SWZ>(smem_u32(kv_smem), C::CB_KV_BYTES, 8 * C::SWZ);
         uint32_t ring = 0, uc = 0;
         uint32_t p_phase = 0;  // bit b: parity of the next p_full[b] completion
         bool ok = true;
@@ -345,8 +403,8 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             for (int kk = 0; kk < D / C::K_STEP; ++kk) {
                 constexpr int step_bytes = C::K_STEP * C::EB;  // along the row
                 const int byte = kk * step_bytes;
-                const uint32_t off_a = ((byte / 128) * C::CB_Q_BYTES + (byte % 128)) >> 4;
-                const uint32_t off_b = ((byte / 128) * C::CB_KV_BYTES + (byte % 128)) >> 4;
+                const uint32_t off_a = ((byte / C::SWZ) * C::CB_Q_BYTES + (byte % C::SWZ)) >> 4;
+                const uint32_t off_b = ((byte / C::SWZ) * C::CB_KV_BYTES + (byte % C::SWZ)) >> 4;
                 mma_ss_warp<F8>(d_t, qa + off_a, kb + off_b, idesc_s, kk > 0 ? 1u : 0u);
             }
         };
@@ -358,15 +416,15 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < C::BN / C::K_STEP; ++kk) {
-                const uint32_t off_b = (kk * C::K_STEP * 128) >> 4;  // K_STEP key rows of 128 B
+                const uint32_t off_b = (kk * C::K_STEP * C::SWZ) >> 4;  // K_STEP key rows of SWZ bytes
                 mma_ts_warp<F8>(d_t, a_t + kk * (C::K_STEP * C::EB / 4), vb + off_b, idesc_o,
                                 kk > 0 ? 1u : acc0);
             }
         };
 
-        for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+        for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
             Unit w;
-            if (!unit_of<C>(su, p, w)) continue;
+            if (!unit_of<C>(su, p, w, tab)) continue;
 #pragma unroll
             for (int i = 0; i < C::NQ; ++i) wait(&bars->q_full[i], uc & 1);
             tc_fence_after_sync();
@@ -458,9 +516,10 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             ++uc;
         }
         if (!ok && lane == 0) raise_timeout(p, bars);
-        // Drain: every MMA this warp issued has finished before TMEM is freed.
+        // Drain: every MMA this warp issued has finished before TMEM is freed (the
+        // fixed cleanup bound: issued MMAs end on their own).
         commit(&bars->drain);
-        mbar_wait(smem_u32(&bars->drain), 0, nullptr, p.timeout_ns);
+        mbar_wait(smem_u32(&bars->drain), 0, nullptr, kCleanupTimeoutNs);
         __syncwarp();
     } else if (warp < C::NUM_SOFTMAX_WARPS) {
         // ------------------------------------------------------------ softmax groups
@@ -481,9 +540,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             return r;
         };
 
-        for (int su = 2 * blockIdx.x; su < 2 * p.num_units && ok; su = next_sub(su)) {
+        for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
             Unit w;
-            if (!unit_of<C>(su, p, w)) continue;
+            if (!unit_of<C>(su, p, w, tab)) continue;
             const int a = w.q0 + grp * C::BM;    // first row of this Q tile
             const int row = a + row_in_tile;     // this thread's query row
             // keys allowed for this row: [jlo, jhi] (positions inside the sequence)
@@ -499,8 +558,18 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             // far instead, dv_ref, and tile t's ratio dv(t) / dv_ref = 2^k (k <= 0, exact)
             // goes into P's exponent: P = e4m3(p * 2^(P8_SHIFT + k)).  O is then rescaled only
             // when the row max or dv_ref grows.
-            float dv_cur = 1.0f, q_desc = 1.0f;
-            if constexpr (F8) q_desc = p.dq[(size_t)w.z * ((p.N + 127) / 128) + a / 128];
+            // fp8: Q and K descales come per block of 2^qk_shift rows (64 or 128; N is a
+            // multiple of 128), V's per 128-row block (one per key tile).  This thread's row
+            // has one Q descale; a key tile's two 64-key halves may have different K
+            // descales, so the score scale c is kept per half (equal when the block is 128).
+            float dv_cur = 1.0f, cq = p.c_log2;
+            const float* dk_head = p.dk;
+            constexpr int QS = C::QK64 ? 6 : 7;   // log2 of the Q / K block rows
+            if constexpr (F8) {
+                const size_t qk_base = (size_t)w.z * (size_t)(p.N >> QS);
+                cq = p.c_log2 * p.dq[qk_base + (row >> QS)];
+                dk_head = p.dk + qk_base;
+            }
 
             int L, R;  // key steps this Q tile needs
             tile_steps<C>(w, grp, p, L, R);
@@ -509,13 +578,16 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 const int t = w.t0 + jj;
                 const int c0 = t * C::BN;
                 const int sb = (C::NQ == 2) ? grp : (jj & 1);
-                float c = p.c_log2;
+                float c = p.c_log2;      // bf16; fp8: c_lo for keys c0 .. c0+63, c_hi above
+                float c_hi = c;
                 float dv_ratio = 1.0f;  // fp8: factor on O before P(t) V8(t) is added
                 int pshift = 0;          // fp8, v_pow2: k = log2(dv(t) / dv_ref) <= 0
                 bool dv_up = false;      // fp8, v_pow2: dv_ref grew at this tile
                 if constexpr (F8) {
-                    const int nkb = (p.N + 127) / 128;
-                    c = p.c_log2 * q_desc * p.dk[(size_t)w.z * nkb + t];
+                    const int nkb = p.N >> 7;
+                    c = cq * dk_head[c0 >> QS];
+                    if constexpr (C::QK64) c_hi = cq * dk_head[(c0 + 64) >> QS];
+                    else c_hi = c;
                     const float dv_t = p.dv[(size_t)w.z * nkb + t];
                     if (!p.v_pow2) {
                         dv_ratio = dv_cur / dv_t;
@@ -558,19 +630,39 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                     }
                 }
                 // row max: 8 independent chains of 3-input maxima, then a small tree
-                float mx[8];
+                // (fp8: one maximum per 64-key half, each scaled by its own c)
+                float m_cand;
+                if constexpr (!C::QK64) {
+                    float mx[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    constexpr int PER = C::BN / 8;
-                    float m = s[k];
+                    for (int k = 0; k < 8; ++k) {
+                        constexpr int PER = C::BN / 8;
+                        float m = s[k];
 #pragma unroll
-                    for (int u2 = 1; u2 + 1 < PER; u2 += 2) m = fmax3(m, s[k + 8 * u2], s[k + 8 * u2 + 8]);
-                    if constexpr (PER % 2 == 0) m = fmaxf(m, s[k + 8 * (PER - 1)]);
-                    mx[k] = m;
+                        for (int u2 = 1; u2 + 1 < PER; u2 += 2) m = fmax3(m, s[k + 8 * u2], s[k + 8 * u2 + 8]);
+                        if constexpr (PER % 2 == 0) m = fmaxf(m, s[k + 8 * (PER - 1)]);
+                        mx[k] = m;
+                    }
+                    const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7]));
+                    m_cand = tmax * c;
+                } else {
+                    float mx[2][8];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float* sh = s + 64 * hf;
+                            mx[hf][k] = fmaxf(fmax3(fmax3(sh[k], sh[k + 8], sh[k + 16]), sh[k + 24], sh[k + 32]),
+                                              fmax3(sh[k + 40], sh[k + 48], sh[k + 56]));
+                        }
+                    float hmax[2];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        hmax[hf] = fmax3(fmax3(mx[hf][0], mx[hf][1], mx[hf][2]),
+                                         fmax3(mx[hf][3], mx[hf][4], mx[hf][5]), fmaxf(mx[hf][6], mx[hf][7]));
+                    m_cand = fmaxf(hmax[0] * c, hmax[1] * c_hi);  // c, c_hi > 0
                 }
-                const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                         fmaxf(mx[6], mx[7]));
-                const float m_cand = tmax * c;
                 const float m_new = fmaxf(m_used, m_cand);
                 // bf16: move the max only when it grew by more than TAU; fp8: always
                 const bool resc = F8 ? (m_new > m_used) : (m_cand > m_used + C::TAU);
@@ -582,6 +674,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 // P = 2^(s*c - m) (fp8: times 2^P8_SHIFT, folded into the exponent)
                 const float mb = (m_used == NEG_INF) ? 0.0f : m_used;
                 const float2 c2 = make_float2(c, c);
+                const float2 c2_hi = C::QK64 ? make_float2(c_hi, c_hi) : c2;
                 const float bias = F8 ? float(C::P8_SHIFT + pshift) - mb : -mb;
                 const float2 b2 = make_float2(bias, bias);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -608,8 +701,9 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             const int i0 = ch * 128 + 4 * e;
-                            const float2 x0 = __ffma2_rn(make_float2(s[i0], s[i0 + 1]), c2, b2);
-                            const float2 x1 = __ffma2_rn(make_float2(s[i0 + 2], s[i0 + 3]), c2, b2);
+                            const float2 ce = (e < 16) ? c2 : c2_hi;  // key half of i0
+                            const float2 x0 = __ffma2_rn(make_float2(s[i0], s[i0 + 1]), ce, b2);
+                            const float2 x1 = __ffma2_rn(make_float2(s[i0 + 2], s[i0 + 3]), ce, b2);
                             const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
                             const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
                             acc[(2 * e) & 3] = __fadd2_rn(acc[(2 * e) & 3], p0);
@@ -677,7 +771,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             if constexpr (F8) inv_l *= dv_cur * (1.0f / float(1u << C::P8_SHIFT));
             const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
             // batched: o[z][row]; packed: o[y0 + row][z] ([T, H, D])
-            const size_t orow_idx = (p.cu_seqlens == nullptr)
+            const size_t orow_idx = (!C::PACKED)
                                         ? (size_t)w.z * p.N + row
                                         : ((size_t)w.y0 + row) * p.H + w.z;
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + orow_idx * D;
@@ -703,13 +797,14 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[grp]));
             if (row < w.N) {
                 const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : NEG_INF;
-                const size_t li = (p.cu_seqlens == nullptr) ? (size_t)w.z * p.N + row
+                const size_t li = (!C::PACKED) ? (size_t)w.z * p.N + row
                                                             : (size_t)w.z * p.T + w.y0 + row;
                 p.lse[li] = lse2 * 0.69314718055994531f;
             }
             ++uc;
         }
         if (!ok) raise_timeout(p, bars);
+        tmem_wait_st();  // an aborted step may have left a P or O store in flight
     } else {
         // ------------------------------------------------------------ spare warps
         if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();

@@ -19,7 +19,15 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
                             const FwdParams& p, int sm_count, cudaStream_t stream)
 {
     using C = FwdCfg<D, F8>;
-    auto kernel = attn_fwd_kernel<D, F8>;
+    // packed variable-length sequences run their own instantiation (bf16 only), so the
+    // batched kernel carries none of their scheduling code
+    auto kernel = attn_fwd_kernel<D, F8, false, false>;
+    if constexpr (!F8) {
+        if (p.cu_seqlens != nullptr) kernel = attn_fwd_kernel<D, F8, true, false>;
+    } else {
+        // 64-row Q/K scale blocks: two K descales per key tile (head-dim-aware scaling)
+        if (p.qk_shift == 6) kernel = attn_fwd_kernel<D, F8, false, true>;
+    }
     // The attribute is per device; setting it is cheap and idempotent.
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

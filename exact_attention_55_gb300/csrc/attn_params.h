@@ -13,6 +13,12 @@ enum : int {
     kStatusTimeout = 5,
 };
 
+// Bound on the waits that only let work already issued finish before shared memory or
+// tensor memory is released after an abort: TMA copies in flight and issued MMAs.
+// Those end within microseconds, so this bound is fixed and independent of the
+// per-wait limit a call sets (which a test may make very short).
+constexpr unsigned long long kCleanupTimeoutNs = 2000000000ull;
+
 struct FwdParams {
     void* o;              // bf16 [BH, N, D]
     float* lse;           // fp32 [BH, N], natural log
@@ -28,8 +34,12 @@ struct FwdParams {
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
     unsigned long long timeout_ns;  // bound on every mbarrier wait
+    int withhold_kv;      // test hook, 0 in every normal call: k > 0 makes each CTA's
+                          // producer skip its K/V load number k - 1 (neither armed nor
+                          // issued), so the waits on it run out and the CTA aborts
     int qk_fmt;           // fp8 path: format of the Q and K codes, 0 E4M3, 1 E5M2 (V is E4M3)
     int v_pow2;           // fp8 path: V's block scales are powers of two (see the softmax)
+    int qk_shift;         // fp8 path: log2 of the rows per Q and K scale block, 6 or 7 (V: 128)
     // Packed variable-length sequences (null cu_seqlens: the batched [BH, N, D] layout).
     // q, k, v, o are [T, H, D]; lse is [H, T]; sequence s is tokens [cu[s], cu[s+1]).
     // Units are (sequence, head, pair of query blocks) with num_qblk from max_seqlen.
@@ -55,6 +65,8 @@ struct BwdParams {
     float c_log2;         // scale * log2(e)
     float scale;
     unsigned long long timeout_ns;
+    int withhold_ring;    // test hook, 0 in every normal call: k > 0 makes each CTA's
+                          // producer skip its ring load number k - 1, so the waits run out
     // Packed variable-length sequences (null cu_seqlens: the batched layout).  Tensors
     // are [T, H, D], lse / delta [H, T]; BH = num_seqs * H, N = max_seqlen, nt from N.
     const int* cu_seqlens;
@@ -90,14 +102,18 @@ struct DecodeParams {
 struct QuantParams {
     const void* x;        // bf16 [BH, N, d]
     uint8_t* x8;          // e4m3 or e5m2 codes [BH, N, d]
-    float* scales;        // fp32 [BH, ceil(N/128)]
+    float* scales;        // fp32 [BH, ceil(N/rows)]
     int* status;          // device status word (timeouts)
     int BH, N, d;
-    int nblk;             // ceil(N / 128)
+    int rows;             // rows per block: 128, or 64 (head-dim-aware scaling at d = 64)
+    int nblk;             // ceil(N / rows)
     int rotate;           // 1: Walsh-Hadamard rotation of each row before quantising
     int fmt;              // 0: E4M3 codes, scale = amax / 448; 1: E5M2, scale = amax / 57344;
                           // 2: E4M3, scale = the smallest power of two >= amax / 448
     float rot_c;          // rotation normalisation fp32(1 / sqrt(d))
+    unsigned long long timeout_ns;  // bound on each wait for a block's load
+    int withhold;         // test hook, 0 in every normal call: k > 0 makes each CTA skip
+                          // the load of its iteration k - 1, so the wait on it runs out
 };
 
 }  // namespace gb300

@@ -149,6 +149,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor for a swizzle span of `swz` bytes: 128 (mode 2, atoms of 8 rows
+// x 128 B, 1024-byte aligned) or 64 (mode 4, atoms of 8 rows x 64 B, 512-byte aligned;
+// the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_64B).
+template <int swz>
+__device__ __forceinline__ uint64_t sdesc_sw(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    static_assert(swz == 128 || swz == 64, "swizzle span");
+    constexpr uint64_t mode = swz == 128 ? 2ull : 4ull;
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (mode << 61);
+}
+
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with an fp32 accumulator:
 //   bits 4-5 D format (1 = f32), bits 7-9 A format, bits 10-12 B format
 //   (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3), bit 15 A major,

@@ -5,7 +5,8 @@
 // onto the FP8 range (largest E4M3 magnitude 448); "大模型加速-核心网络算子-
 // Flash Attention V3", §1 item 3 / §1.5: block quantisation into E4M3.
 //
-// For each (head, block of 128 rows, all d columns):
+// For each (head, block of 128 rows -- or 64, the head-dim-aware block of Q and K at
+// d = 64 -- all d columns):
 //   amax  = max |x|;  scale = amax / 448 (IEEE fp32 division), or 1 when amax == 0
 //   x8    = e4m3_rn_satfinite(x / scale)   (IEEE fp32 quotient, one rounding to E4M3)
 // The E5M2 variant (the pages' wider-range format, "大模型加速-核心网络算子-Flash
@@ -56,7 +57,6 @@ __host__ __device__ constexpr int quant_smem_bytes(int d)
 {
     return 128 + kQuantStages * kQuantRows * d * 2 + 64;
 }
-constexpr unsigned long long kQuantTimeoutNs = 4000000000ull;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -137,11 +137,16 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
     const int total = p.BH * p.nblk;
     const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(p.x);
 
-    auto block_rows = [&](int blk) { return min(kQuantRows, p.N - (blk % p.nblk) * kQuantRows); };
+    // blocks of p.rows rows (128, or 64); a stage holds the largest block, 128 rows
+    auto block_rows = [&](int blk) { return min(p.rows, p.N - (blk % p.nblk) * p.rows); };
     auto block_base = [&](int blk) {  // element offset of the block
-        return ((size_t)(blk / p.nblk) * p.N + (size_t)(blk % p.nblk) * kQuantRows) * p.d;
+        return ((size_t)(blk / p.nblk) * p.N + (size_t)(blk % p.nblk) * p.rows) * p.d;
     };
-    auto issue = [&](int blk, int stage) {
+    // load the block of iteration `j` of this CTA into its stage (the test hook withholds
+    // one iteration's load: its wait then runs out)
+    auto issue = [&](int j) {
+        if (j + 1 == p.withhold) return;
+        const int blk = blockIdx.x + j * gridDim.x, stage = j % kQuantStages;
         const uint32_t bytes = (uint32_t)block_rows(blk) * p.d * 2;
         const uint32_t bar = smem_u32(&full[stage]);
         mbar_arrive_expect_tx(bar, bytes);
@@ -152,10 +157,8 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
         for (int s = 0; s < kQuantStages; ++s) mbar_init(smem_u32(&full[s]), 1);
         abort_flag = 0;
         fence_mbar_init();
-        for (int s = 0; s < kQuantStages; ++s) {
-            const int blk = blockIdx.x + s * gridDim.x;
-            if (blk < total) issue(blk, s);
-        }
+        for (int s = 0; s < kQuantStages; ++s)
+            if (blockIdx.x + s * gridDim.x < total) issue(s);
     }
     __syncthreads();
 
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
     for (int blk = blockIdx.x; blk < total; blk += gridDim.x, ++it) {
         const int stage = it % kQuantStages;
         const uint32_t parity = (it / kQuantStages) & 1;
-        bool ok = mbar_wait(smem_u32(&full[stage]), parity, &abort_flag, kQuantTimeoutNs);
+        bool ok = mbar_wait(smem_u32(&full[stage]), parity, &abort_flag, p.timeout_ns);
         if (!__syncthreads_and(ok)) {
             if (threadIdx.x == 0) {
                 abort_flag = 1;
@@ -310,21 +313,21 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
         // every thread is done with this stage (and with warp_max) before it is refilled
         __syncthreads();
         if (threadIdx.x == 0) {
-            const int next = blk + kQuantStages * gridDim.x;
-            if (next < total) {
+            if (blk + kQuantStages * gridDim.x < total) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(next, stage);
+                issue(it + kQuantStages);
             }
         }
     }
-    // Let every copy this CTA issued land before its shared memory is released.
+    // Let every copy this CTA issued land before its shared memory is released (copies
+    // end on their own: the fixed cleanup bound, not the per-wait limit).
     if (threadIdx.x == 0 && abort_flag) {
         for (int k = 0; k < kQuantStages; ++k) {
             const int j = it + k;  // loads issued for iterations it .. it+stages-1
             const int blk = blockIdx.x + j * gridDim.x;
-            if (blk < total)
+            if (blk < total && j + 1 != p.withhold)
                 mbar_wait(smem_u32(&full[j % kQuantStages]), (j / kQuantStages) & 1, nullptr,
-                          kQuantTimeoutNs);
+                          kCleanupTimeoutNs);
         }
     }
 }
@@ -345,6 +348,45 @@ static cudaError_t launch_quant(const QuantParams& p, int sm_count, cudaStream_t
     const long long want = (long long)sm_count * per_sm;
     const int grid = total < want ? total : (int)want;
     kernel<<<grid, QuantShape<DR>::kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Diagnostic: the FP8 conversion the quantiser uses (pack_e4m3x2 / pack_e5m2x2), applied to
+// the fp32 bit patterns first .. first + count - 1 (count a multiple of 8): codes[i] is the
+// code of the float whose bits are first + i.  Lets a test compare the device conversion
+// with an independent encoder over every fp32 pattern.
+template <int FMT>
+__global__ void __launch_bounds__(256) fp8_convert_kernel(uint32_t first, size_t count8, uint2* codes)
+{
+    for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < count8;
+         g += (size_t)gridDim.x * blockDim.x) {
+        const uint32_t b0 = first + (uint32_t)(8 * g);
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float f[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f[k] = __uint_as_float(b0 + 4 * h + k);
+            const uint32_t lo = FMT == 1 ? pack_e5m2x2(f[0], f[1]) : pack_e4m3x2(f[0], f[1]);
+            const uint32_t hi = FMT == 1 ? pack_e5m2x2(f[2], f[3]) : pack_e4m3x2(f[2], f[3]);
+            w[h] = lo | (hi << 16);
+        }
+        codes[g] = make_uint2(w[0], w[1]);
+    }
+}
+
+cudaError_t launch_fp8_convert(uint32_t first, size_t count, int fmt, void* codes, int sm_count,
+                               cudaStream_t stream)
+{
+    const size_t count8 = count / 8;
+    size_t blocks = (count8 + 255) / 256;
+    const size_t cap = (size_t)sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (fmt == 1)
+        fp8_convert_kernel<1><<<(unsigned)blocks, 256, 0, stream>>>(first, count8, static_cast<uint2*>(codes));
+    else
+        fp8_convert_kernel<0><<<(unsigned)blocks, 256, 0, stream>>>(first, count8, static_cast<uint2*>(codes));
     return cudaGetLastError();
 }
 

@@ -214,7 +214,8 @@ attn_status_t attn_decode_bf16_paged_noalloc(const void* q, const void* k_cache,
  *   x      : const bf16 [B, H, N, d]
  *   x8     : uint8 (E4M3 codes) [B, H, N, d], written
  *   scales : float [B, H, ceil(N / block)], written; x ~= x8 * scales[block of row]
- *   block  : must be 128 (else ATTN_ERR_UNSUPPORTED); d % 16 == 0 and d <= 256
+ *   block  : 128, or 64 (the head-dim-aware block of Q and K at d = 64, see
+ *            attn_fp8_qk_block_rows); else ATTN_ERR_UNSUPPORTED.  d % 16 == 0, d <= 256
  */
 attn_status_t attn_quantize_fp8_blockwise(const void* x, void* x8, float* scales, int B, int H,
                                           int N, int d, int block, void* stream);
@@ -266,7 +267,7 @@ attn_status_t attn_quantize_fp8_blockwise_fmt(const void* x, void* x8, float* sc
  *   descale_q/k/v : const float [B, H, N / 128], the matching `scales`
  *                   (x ~= x8 * descale for the 128-row block of the row)
  *   o, lse, scale, causal, window : as attn_fwd_bf16
- *   d in {128, 256}; N % 128 == 0 (else ATTN_ERR_UNSUPPORTED)
+ *   d in {64, 128, 256}; N % 128 == 0 (else ATTN_ERR_UNSUPPORTED)
  * Scores are descaled per (query block, key block) inside the softmax.  P is
  * rounded to E4M3 as p * 2^8 (p <= 1 against the exact running maximum); the V
  * descale of each key block is applied to the fp32 O accumulator, which is
@@ -297,6 +298,38 @@ attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const void* v8,
                                int d, float scale, int causal, int window, int qk_format,
                                int v_format, void* stream);
 
+/*
+ * attn_fp8_qk_block_rows -- rows per Q and K scale block under head-dim-aware
+ * scaling: min(d, 128) (0 for d < 1).
+ *
+ * [WGC] §3 FP8 量化与精度保持 (头维度感知量化): the scaling is tuned separately for
+ * head dims 64 and 128 so that small head dims do not lose precision; no rule is
+ * given.  Reading: Q and K, whose products run over the d entries of a row, get
+ * blocks of min(d, 128) rows -- 64 at d = 64, the 128 rows of the FP8 workload at
+ * d >= 128 -- and V keeps 128-row blocks at every d (its error in O averages over
+ * keys, not over d).  On the FP8 workload's distribution at d = 64 this lowers the
+ * error against unquantised attention; 64-row V blocks change nothing measurable.
+ */
+int attn_fp8_qk_block_rows(int d);
+
+/*
+ * attn_fwd_fp8_blocks -- attn_fwd_fp8_fmt with the height of the Q and K scale blocks
+ * as a parameter, for head-dim-aware scaling.
+ *   qk_block      : 64 or 128 (else ATTN_ERR_UNSUPPORTED): rows per scale block of Q
+ *                   and K; attn_fp8_qk_block_rows(d) gives the head-dim-aware value
+ *   descale_q, descale_k : const float [B, H, N / qk_block], the `scales` that
+ *                   attn_quantize_fp8_blockwise(_fmt) wrote with block = qk_block
+ *   descale_v     : const float [B, H, N / 128] (V is quantised with block = 128)
+ * A 128-key tile then spans two K blocks when qk_block = 64; the softmax applies each
+ * 64-key half's descale to its own scores.  qk_block = 128 is exactly attn_fwd_fp8_fmt.
+ * Other arguments and errors as attn_fwd_fp8_fmt.
+ */
+attn_status_t attn_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8,
+                                  const float* descale_q, const float* descale_k,
+                                  const float* descale_v, void* o, float* lse, int B, int H,
+                                  int N, int d, float scale, int causal, int window,
+                                  int qk_format, int v_format, int qk_block, void* stream);
+
 /* Static English text for a status code (never NULL). */
 const char* attn_status_string(attn_status_t status);
 
@@ -318,6 +351,52 @@ attn_status_t attn_get_device_status(void* stream);
  *   timeout_ns : 1 .. 2e9 (else ATTN_ERR_INVALID_ARG)
  */
 attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream);
+
+/*
+ * attn_selftest_fwd_withheld_load, attn_selftest_quant_withheld_load,
+ * attn_selftest_bwd_withheld_load -- diagnostics for the abort path of the real
+ * kernels (no page describes them: they test this library's failure detection).
+ * Each runs the production kernel of attn_fwd_bf16 (scale 1/sqrt(d), no window),
+ * of attn_quantize_fp8_blockwise (E4M3, block 128) or of attn_bwd_bf16 on the
+ * given tensors, with two differences: every wait is bounded by `timeout_ns`
+ * instead of the usual 4 s, and in every CTA the load with index `withheld`
+ * (0-based, counted over that CTA's K/V tiles, its 128-row blocks, or its
+ * backward ring tiles) is never issued.  The waits on it run out; the CTA raises
+ * its abort flag, lets the copies and MMAs it already issued finish, frees its
+ * tensor memory and exits, and ATTN_ERR_TIMEOUT is recorded for
+ * attn_get_device_status().  The outputs are then unspecified; the context stays
+ * usable.  A CTA that never reaches load `withheld` finishes normally.
+ * Arguments are as for the production entry points, plus
+ *   withheld   : >= 0
+ *   timeout_ns : 1 .. 2e9 (else ATTN_ERR_INVALID_ARG)
+ */
+attn_status_t attn_selftest_fwd_withheld_load(const void* q, const void* k, const void* v,
+                                              void* o, float* lse, int B, int H, int N, int d,
+                                              int causal, int withheld,
+                                              unsigned long long timeout_ns, void* stream);
+attn_status_t attn_selftest_quant_withheld_load(const void* x, void* x8, float* scales, int B,
+                                                int H, int N, int d, int withheld,
+                                                unsigned long long timeout_ns, void* stream);
+attn_status_t attn_selftest_bwd_withheld_load(const void* q, const void* k, const void* v,
+                                              const void* o, const void* dout, const float* lse,
+                                              void* dq, void* dk, void* dv, void* workspace,
+                                              size_t workspace_bytes, int B, int H, int N, int d,
+                                              int causal, int withheld,
+                                              unsigned long long timeout_ns, void* stream);
+
+/*
+ * attn_selftest_fp8_convert -- diagnostic: the device's FP8 conversion (the one the
+ * quantisers use: round to nearest even, saturating to the format's largest finite
+ * value) applied to the fp32 bit patterns first .. first + count - 1, so that a test
+ * can compare it with an independent encoder over all 2^32 patterns.  [JJ] §1.5
+ * (E4M3 and E5M2).
+ *   codes  : uint8 [count] on the device, 16-byte aligned, written: codes[i] is the
+ *            code of the float whose bit pattern is first + i
+ *   count  : a positive multiple of 8 with first + count <= 2^32
+ *   format : ATTN_FP8_E4M3 or ATTN_FP8_E5M2 (else ATTN_ERR_INVALID_ARG)
+ */
+attn_status_t attn_selftest_fp8_convert(unsigned int first, size_t count, int format,
+                                        void* codes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -65,12 +65,12 @@ def assert_bf16_close(o_gpu, lse_gpu, o_ref, lse_ref, label=""):
 
 def fp8_lse_bound(lse_ref):
     """Per-row bound on |LSE_kernel - LSE_oracle| for the FP8 path against the oracle
-    on the dequantised inputs: 1e-3 (the specification's LSE bar) relative to
-    max(1, |LSE|).  Both sides see the same dequantised scores; the kernel holds them
-    in fp32 (exact E4M3 products accumulated by the tensor core, then one product
-    with the fp32 descale scale * log2(e) * dq * dk), so its LSE error grows with the
-    score magnitude, which outliers raise to a few hundred on the FP8 workload."""
-    return 1e-3 * np.maximum(1.0, np.abs(lse_ref))
+    on the dequantised inputs: the specification's LSE bar, 1e-3.  Against those
+    inputs the FP8 kernel evaluates the same scores as the oracle up to fp32 rounding:
+    each product of two E4M3 (or E5M2) codes is exact in fp32, the tensor core sums
+    them in fp32, and the block descales enter through one fp32 product, the same
+    softmax arithmetic the bf16 path runs against its own bar."""
+    return np.full(np.shape(lse_ref), LSE_MAX_ABS)
 
 
 def rel_rmse(a, ref):

@@ -86,7 +86,8 @@ def test_bf16_argument_errors(lib, args, expected):
 
 @pytest.mark.parametrize("args,expected", [
     ((0, P, P, 1, 1, 128, 128, 128), 1),
-    ((P, P, P, 1, 1, 128, 128, 64), 2),      # block != 128
+    ((P, P, P, 1, 1, 128, 128, 32), 2),      # block not 64 or 128
+    ((P, P, P, 1, 1, 128, 128, 256), 2),
     ((P, P, P, 1, 1, 128, 120, 128), 2),     # d % 16 != 0
     ((P, P, P, 1, 1, 128, 512, 128), 2),     # d > 256
     ((P + 4, P, P, 1, 1, 128, 128, 128), 3),
@@ -99,7 +100,7 @@ def test_quantizer_argument_errors(lib, args, expected):
 @pytest.mark.parametrize("args,expected", [
     ((P, P, P, 0, P, P, P, P, 1, 1, 256, 128, 0.1, 0, 0), 1),   # null descale
     ((P, P, P, P, P, P, P, P, 1, 1, 200, 128, 0.1, 0, 0), 2),   # N % 128
-    ((P, P, P, P, P, P, P, P, 1, 1, 256, 64, 0.1, 0, 0), 2),    # d = 64
+    ((P, P, P, P, P, P, P, P, 1, 1, 256, 32, 0.1, 0, 0), 2),    # d = 32
     ((P, P, P + 1, P, P, P, P, P, 1, 1, 256, 128, 0.1, 0, 0), 3),
 ])
 def test_fp8_argument_errors(lib, args, expected):
@@ -109,6 +110,15 @@ def test_fp8_argument_errors(lib, args, expected):
 def test_selftest_rejects_bad_limits_before_any_launch(lib):
     assert lib.attn_selftest_wait_timeout(0, None) == 1
     assert lib.attn_selftest_wait_timeout(3_000_000_000, None) == 1
+    fwd = (P, P, P, P, P, 1, 1, 256, 128, 0)
+    assert lib.attn_selftest_fwd_withheld_load(*fwd, -1, 1_000_000, None) == 1
+    assert lib.attn_selftest_fwd_withheld_load(*fwd, 2, 0, None) == 1
+    assert lib.attn_selftest_fwd_withheld_load(*fwd, 2, 3_000_000_000, None) == 1
+    assert lib.attn_selftest_quant_withheld_load(P, P, P, 1, 1, 256, 128, -1, 1_000_000, None) == 1
+    assert lib.attn_selftest_quant_withheld_load(P, P, P, 1, 1, 256, 128, 0, 0, None) == 1
+    bwd = (P, P, P, P, P, P, P, P, P, P, 4096, 1, 1, 256, 128, 0)
+    assert lib.attn_selftest_bwd_withheld_load(*bwd, -1, 1_000_000, None) == 1
+    assert lib.attn_selftest_bwd_withheld_load(*bwd, 1, 0, None) == 1
 
 
 def test_binding_refuses_cpu_tensors():
@@ -133,7 +143,7 @@ def test_missing_library_fails_loudly(tmp_path):
 @pytest.mark.parametrize("args,expected", [
     ((P, P, P, 1, 1, 128, 128, 128, 3), 1),       # unknown format
     ((P, P, P, 1, 1, 128, 128, 128, -1), 1),
-    ((P, P, P, 1, 1, 128, 128, 64, 1), 2),        # E5M2, block != 128
+    ((P, P, P, 1, 1, 128, 128, 96, 1), 2),        # E5M2, block not 64 or 128
     ((P + 4, P, P, 1, 1, 128, 128, 128, 2), 3),   # power-of-two scales, x misaligned
 ])
 def test_quantizer_fmt_argument_errors(lib, args, expected):
@@ -145,12 +155,28 @@ def test_quantizer_fmt_argument_errors(lib, args, expected):
     ((0, 1), (256, 128), 1),      # V in E5M2 is not a V format
     ((1, 3), (256, 128), 1),
     ((1, 0), (200, 128), 2),      # E5M2 Q/K, N % 128
-    ((0, 2), (256, 64), 2),       # power-of-two V, d = 64
+    ((0, 2), (256, 96), 2),       # power-of-two V, d = 96
 ])
 def test_fp8_fmt_argument_errors(lib, fmts, shape, expected):
     N, d = shape
     args = (P, P, P, P, P, P, P, P, 1, 1, N, d, 0.1, 0, 0)
     assert lib.attn_fwd_fp8_fmt(*args, *fmts, None) == expected
+
+
+@pytest.mark.parametrize("qk_block,shape,expected", [
+    (32, (256, 64), 2),           # block height not 64 or 128
+    (256, (256, 128), 2),
+    (64, (200, 64), 2),           # N % 128
+    (64, (256, 48), 2),           # head dim
+])
+def test_fp8_blocks_argument_errors(lib, qk_block, shape, expected):
+    N, d = shape
+    args = (P, P, P, P, P, P, P, P, 1, 1, N, d, 0.1, 0, 0, 0, 0, qk_block)
+    assert lib.attn_fwd_fp8_blocks(*args, None) == expected
+
+
+def test_head_dim_aware_block_rows(lib):
+    assert [lib.attn_fp8_qk_block_rows(d) for d in (64, 128, 256, 0)] == [64, 128, 128, 0]
 
 
 def test_bwd_workspace_size(lib):

@@ -98,3 +98,25 @@ def test_mixed_lengths_at_headline_token_count(fa, causal):
             o_g = o[a:b, h][rows].double().numpy()
             l_g = lse[h, a:b][rows].double().numpy()
             assert_bf16_close(o_g, l_g, o_ref, l_ref, f"seq {s} (n={n}) head {h}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_more_sequences_than_the_schedule_table(fa, causal):
+    """Up to 220 sequences are scheduled longest first from a table each CTA sorts; more
+    fall back to the round-robin over pair slots.  Both paths against the oracle, and
+    both bit-identical to a call on the same sequences one at a time."""
+    g = torch.Generator().manual_seed(55)
+    for count in (219, 221, 300):
+        lengths = torch.randint(0, 300, (count,), generator=g).tolist()
+        lengths[count // 2] = 700                  # one long sequence among short ones
+        q, k, v, cu = make_packed_qkv(lengths, 2, 64, seed=56)
+        o, lse = _run(fa, q, k, v, cu, 0.125, causal, 0)
+        o_ref, lse_ref = oracle.attn_varlen_f64(q, k, v, cu.numpy(), 0.125, causal=causal)
+        assert_bf16_close(o.double().numpy(), lse.double().numpy(), o_ref, lse_ref,
+                          f"{count} sequences causal={causal}")
+        s = count // 2
+        a, b = int(cu[s]), int(cu[s + 1])
+        one = torch.tensor([0, b - a], dtype=torch.int32)
+        o1, l1 = _run(fa, q[a:b].contiguous(), k[a:b].contiguous(), v[a:b].contiguous(), one,
+                      0.125, causal, 0)
+        assert torch.equal(o[a:b], o1) and torch.equal(lse[:, a:b], l1)
