@@ -499,6 +499,25 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
         "bar": 4e-2, **bars,
         "against": "attn_fwd_bf16 on the same (unquantised) bf16 inputs, all 256 heads"}
     del o_fp8, o_ref
+    # the sweep's weakest points as bf16 lines: head dim 64 at N = 16384 (B1 H32), non-causal
+    # and causal with a 1024-key window, and head dim 128 with that window (B1 H16)
+    for dd, hh in ((64, 32), (128, 16)):
+        qw, kw, vw = (t.to(dev) for t in make_qkv(1, hh, 16384, dd, seed=7))
+        ow = torch.empty_like(qw)
+        lw = torch.empty((1, hh, 16384), dtype=torch.float32, device=dev)
+        for causal, window in ((False, 0), (True, 1024)):
+            if dd == 128 and not causal:
+                continue
+            def sweep_step():
+                fa.attn_fwd_bf16(qw, kw, vw, scale=1.0 / math.sqrt(dd), causal=causal, window=window,
+                                 o=ow, lse=lw, stream=stream)
+            ms, per = time_steps(sweep_step, reps, 3, stream)
+            f = 4.0 * dd * hh * allowed_pairs(16384, causal, window)
+            key = f"bf16_d{dd}_n16384" + ("_causal_w1024" if window else "")
+            out[key] = {"tflops": f / (statistics.mean(per) * 1e-3) / 1e12,
+                        "ms": statistics.mean(per), "shape": f"B1 H{hh} N16384 d{dd}",
+                        "flops": "4 d per allowed (query, key) pair"}
+        del qw, kw, vw, ow, lw
     # FP8 at head dim 64 with head-dim-aware scaling (Q, K per 64-row block, V per 128):
     # the FP8 workload's distribution at B16 H16 N8192 d64
     q6, k6, v6 = make_qkv(B, H, N, 64, seed=0, outliers=True)
@@ -575,7 +594,24 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
     gbs = dbytes / (statistics.mean(per) * 1e-3) / 1e9
     out["decode_paged_noalloc"] = {"GB_per_s": gbs, "frac_of_hbm": gbs / hbm,
                                    "us": 1e3 * statistics.mean(per)}
-    del dq_, dkc, dvc, dpt, dsl, do_, dl_, dws
+    # several new tokens per sequence (speculative / multi-token decoding): the tensor-core
+    # kernel, same cache, nq = 4
+    dq4 = torch.randn((B, H, 4, D), device=dev).to(torch.bfloat16)
+    do4 = torch.empty_like(dq4)
+    dl4 = torch.empty((B, H, 4), dtype=torch.float32, device=dev)
+    nws4 = fa.attn_decode_workspace_bytes(B, H, 4, D, 64, dpt.shape[1], 0)
+    dws4 = torch.empty(max(nws4 // 4, 1), dtype=torch.float32, device=dev)
+
+    def decode4_step():
+        fa.attn_decode_bf16_paged(dq4, dkc, dvc, dpt, dsl, scale=scale, workspace=dws4, o=do4,
+                                  lse=dl4, stream=stream)
+    ms, per = time_steps(decode4_step, reps, 3, stream)
+    dbytes4 = 2 * B * H * N * D * 2 + 2 * dq4.numel() * 2 + dl4.numel() * 4
+    gbs = dbytes4 / (statistics.mean(per) * 1e-3) / 1e9
+    out["decode_paged_nq4"] = {"GB_per_s": gbs, "frac_of_hbm": gbs / hbm,
+                               "us": 1e3 * statistics.mean(per), "bytes": dbytes4,
+                               "shape": "B16 H16 L8192 d128 nq4, 64-token pages (tensor cores)"}
+    del dq_, dkc, dvc, dpt, dsl, do_, dl_, dws, dq4, do4, dl4, dws4
     # backward pass on the headline shape: dO seeded on the device; FLOPs counted as
     # 2.5 x the forward's (five N x N x d products), halved under the causal mask; the
     # kernels run seven such products (S is recomputed in both passes)
@@ -671,12 +707,28 @@ def run_profile_case(args):
 
         def run():
             fa.attn_bwd_bf16(qd, kd, vd, o, dout, lse, scale=scale)
-    elif args.profile == "decode":
+    elif args.profile in ("decode", "decode_nq4"):
         from exact_attention_55_gb300.inputs import make_paged_cache
-        dq_, dkc, dvc, dpt, dsl = (t.cuda() for t in make_paged_cache([n] * 8, h, 1, d, 64, seed=0))
+        nq = 4 if args.profile == "decode_nq4" else 1
+        dq_, dkc, dvc, dpt, dsl = (t.cuda() for t in make_paged_cache([n] * 8, h, nq, d, 64, seed=0))
 
         def run():
             fa.attn_decode_bf16_paged(dq_, dkc, dvc, dpt, dsl, scale=scale)
+    elif args.profile == "varlen":
+        from exact_attention_55_gb300.inputs import make_packed_qkv, varlen_lengths
+        lengths = varlen_lengths(b * n, 512, 8192, seed=3)
+        qp, kp, vp, cu = (t.cuda() for t in make_packed_qkv(lengths, h, d, seed=0))
+
+        def run():
+            fa.attn_fwd_bf16_varlen(qp, kp, vp, cu, max(lengths), scale=scale)
+    elif args.profile == "fp8_d64":
+        q6, k6, v6 = (t.cuda() for t in make_qkv(b, h, n, 64, seed=0, outliers=True))
+        qs = [fa.attn_quantize_fp8_blockwise(t, block=64) for t in (q6, k6)]
+        vs = fa.attn_quantize_fp8_blockwise(v6, block=128)
+
+        def run():
+            fa.attn_fwd_fp8_blocks(qs[0][0], qs[1][0], vs[0], qs[0][1], qs[1][1], vs[1], qk_block=64,
+                                   scale=0.125)
     else:
         qs = [fa.attn_quantize_fp8_blockwise(t) for t in (qd, kd, vd)]
 
@@ -753,8 +805,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline kernel timing only")
     ap.add_argument("--profile", default=None,
-                    choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "quant",
-                             "quant_hadamard", "decode", "bwd"],
+                    choices=["bf16", "bf16_causal", "fp8", "fp8_causal", "fp8_d64", "quant",
+                             "quant_hadamard", "decode", "decode_nq4", "varlen", "bwd"],
                     help="run a small case of one kernel (for ncu) and exit")
     ap.add_argument("--sweep", action="store_true",
                     help="time the d x N x mask sweep (one JSON line per point) and exit")

@@ -28,6 +28,7 @@ UNITS = [
     ("api", "api.cu", []),
     ("quant_fp8", "quant_fp8.cu", []),
     ("decode", "decode.cu", []),
+    ("decode_tc", "decode_tc.cu", []),
     ("attn_bwd", "attn_bwd.cu", []),
     ("fwd_bf16_d64", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=64", "-DGB300_ATTN_F8=0"]),
     ("fwd_bf16_d128", "attn_fwd_inst.cu", ["-DGB300_ATTN_D=128", "-DGB300_ATTN_F8=0"]),

@@ -23,6 +23,8 @@ cudaError_t launch_quant_fp8(const QuantParams& p, int sm_count, cudaStream_t st
 cudaError_t launch_fp8_convert(uint32_t first, size_t count, int fmt, void* codes, int sm_count,
                                cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream);
+cudaError_t launch_decode_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                             const DecodeParams& p, int d, int sm_count, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdMaps& m, const BwdParams& p, int d, int sm_count, cudaStream_t stream);
 
 // One status word per device: kernels write kStatusTimeout here when they give up.
@@ -244,6 +246,44 @@ void decode_plan(int BH, int max_pages, int log2_ps, int requested, int sm_count
     if (want > max_pages) want = max_pages;
     *pps = (int)((max_pages + want - 1) / want);
     *splits = (max_pages + *pps - 1) / *pps;
+}
+
+// The tensor-core decoding kernel (decode_tc.cu) takes steps of 2 to 8 queries at head dims
+// 64 and 128 with pages of at least 8 rows (one TMA box per page); nq = 1, d = 256 and tiny
+// pages stay on the CUDA-core kernel.
+bool decode_uses_tc(int nq, int d, int log2_ps)
+{
+    return nq >= 2 && (d == 64 || d == 128) && log2_ps >= 3;
+}
+
+// Split plan of the tensor-core kernel: splits hold whole 128-key tiles; 0 aims at about
+// eight (head, split) units per CTA of the persistent grid with at least two tiles each;
+// requested > 0 is honoured up to whole tiles (never more splits than requested).
+void decode_plan_tc(int BH, int max_pages, int log2_ps, int requested, int sm_count, int* splits,
+                    int* pps)
+{
+    const long long tiles = (((long long)max_pages << log2_ps) + 127) / 128;
+    long long want = (8LL * sm_count + BH - 1) / BH;
+    if (want > (tiles + 1) / 2) want = (tiles + 1) / 2;
+    if (requested > 0) want = requested;
+    if (want < 1) want = 1;
+    if (want > tiles) want = tiles;
+    const long long tps = (tiles + want - 1) / want;                  // tiles per split
+    long long pages = log2_ps >= 7 ? (tps * 128 + (1LL << log2_ps) - 1) >> log2_ps
+                                   : tps << (7 - log2_ps);            // keys: a multiple of 128
+    if (pages > max_pages) pages = max_pages;                          // then one split
+    if (pages < 1) pages = 1;
+    *pps = (int)pages;
+    *splits = (int)((max_pages + pages - 1) / pages);
+}
+
+void decode_plan_any(int BH, int nq, int d, int max_pages, int log2_ps, int requested,
+                     int sm_count, int* splits, int* pps)
+{
+    if (decode_uses_tc(nq, d, log2_ps))
+        decode_plan_tc(BH, max_pages, log2_ps, requested, sm_count, splits, pps);
+    else
+        decode_plan(BH, max_pages, log2_ps, requested, sm_count, splits, pps);
 }
 
 int page_log2(int page_size)
@@ -554,7 +594,8 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int H, int nq, int d, int p
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != ATTN_OK) return 0;
     int splits = 1, pps = 1;
-    decode_plan(B * H, max_pages, page_log2(page_size), num_splits, dev->sm_count, &splits, &pps);
+    decode_plan_any(B * H, nq, d, max_pages, page_log2(page_size), num_splits, dev->sm_count,
+                    &splits, &pps);
     return decode_ws_bytes((long long)B * H, splits, nq, d);
 }
 
@@ -587,15 +628,19 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     }
     const long long BH = (long long)B * H;
     const int lg = page_log2(page_size);
+    const bool tc = decode_uses_tc(nq, d, lg);
+    if (tc && (long long)num_pages * H > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;  // TMA rows
     int splits = 1, pps = 1;
-    decode_plan((int)BH, max_pages, lg, num_splits, dev->sm_count, &splits, &pps);
+    decode_plan_any((int)BH, nq, d, max_pages, lg, num_splits, dev->sm_count, &splits, &pps);
     if (decode_ws_bytes(BH, splits, nq, d) > (workspace ? workspace_bytes : 0)) {
         if (num_splits > 0) return ATTN_ERR_INVALID_ARG;   // asked for more than fits
         // automatic plan: fall back to as many splits as the workspace holds
         const long long per = BH * nq * (d + 1) * (long long)sizeof(float);
         const long long fit = workspace ? (long long)(workspace_bytes / per) : 1;
-        decode_plan((int)BH, max_pages, lg, fit > 1 ? (int)fit : 1, dev->sm_count, &splits, &pps);
+        decode_plan_any((int)BH, nq, d, max_pages, lg, fit > 1 ? (int)fit : 1, dev->sm_count,
+                        &splits, &pps);
     }
+    if (tc && BH * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;   // (head, split) units
     DecodeParams p;
     std::memset(&p, 0, sizeof(p));
     p.q = q;
@@ -615,6 +660,23 @@ static attn_status_t decode_paged(const void* q, const void* k_cache, const void
     p.splits = splits;
     p.pages_per_split = pps;
     p.c_log2 = (float)((double)scale * 1.4426950408889634);
+    p.status = dev->status;
+    p.timeout_ns = kWaitTimeoutNs;
+    if (tc) {
+        // Q as (d, nq, B*H) with nq-row boxes; the caches as (d, page_size, pages * H) with
+        // boxes of one page (or 128 rows of a larger page): a page of one head is contiguous
+        alignas(64) CUtensorMap mq, mk, mv;
+        const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const int rows = page_size < 128 ? page_size : 128;
+        if (!encode_3d(&mq, q, dt, 2, d, nq, (int)BH, nq) ||
+            !encode_3d(&mk, k_cache, dt, 2, d, page_size, num_pages * H, rows) ||
+            !encode_3d(&mv, v_cache, dt, 2, d, page_size, num_pages * H, rows))
+            return ATTN_ERR_CUDA;
+        if (launch_decode_tc(mq, mk, mv, p, d, dev->sm_count, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+            return ATTN_ERR_CUDA;
+        return ATTN_OK;
+    }
     if (launch_decode(p, d, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;

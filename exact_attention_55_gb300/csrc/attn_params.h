@@ -97,6 +97,8 @@ struct DecodeParams {
     int num_pages, max_pages;
     int splits, pages_per_split;
     float c_log2;         // softmax scale * log2(e)
+    int* status;          // device status word (the tensor-core kernel's bounded waits)
+    unsigned long long timeout_ns;
 };
 
 struct QuantParams {

@@ -302,6 +302,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     if (lane == 0) p.lse[qi] = wsum > 0.0f ? (M + __log2f(wsum)) * 0.69314718055994531f : NEG_INF;
 }
 
+// Merge the split partials in p.ws into o and lse (also used by the tensor-core kernel).
+cudaError_t launch_decode_combine(const DecodeParams& p, int d, cudaStream_t stream)
+{
+    const long long rows = (long long)p.B * p.H * p.nq;
+    const unsigned grid = (unsigned)((rows + 3) / 4);
+    switch (d) {
+    case 64: decode_combine_kernel<64><<<grid, 128, 0, stream>>>(p); break;
+    case 128: decode_combine_kernel<128><<<grid, 128, 0, stream>>>(p); break;
+    case 256: decode_combine_kernel<256><<<grid, 128, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 template <int D, int NQ>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream)
 {
@@ -309,9 +323,7 @@ static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream)
     decode_split_kernel<D, NQ><<<grid, kDecWarps * 32, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.splits == 1) return e;
-    const long long rows = (long long)p.B * p.H * p.nq;
-    decode_combine_kernel<D><<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_decode_combine(p, D, stream);
 }
 
 template <int D>

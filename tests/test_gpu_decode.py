@@ -46,6 +46,24 @@ def test_full_size_step(fa):
     _check(fa, [8192] * 16, 16, 1, 128, 64, 0, seed=0, label="B16 H16 L8192")
 
 
+@pytest.mark.parametrize("nq", [2, 4, 8])
+def test_full_size_multi_query_step(fa, nq):
+    """B=16, H=16, 8192 cached tokens each in 64-token pages, d=128, nq new tokens (the
+    tensor-core kernel): every output against the oracle."""
+    _check(fa, [8192] * 16, 16, nq, 128, 64, 0, seed=nq, label=f"B16 H16 L8192 nq{nq}")
+
+
+@pytest.mark.parametrize("ps", [8, 128, 256])
+def test_multi_query_page_sizes(fa, ps):
+    """Pages smaller than, equal to and larger than a 128-key tile, lengths that end inside
+    a tile and inside a page, d = 64 and 128, automatic and forced splits."""
+    lens = [1, 7, 127, 128, 129, 300, 1000, 2049]
+    for d in (64, 128):
+        for splits in (0, 1, 3):
+            _check(fa, [max(4, n) for n in lens], 2, 4, d, ps, splits, seed=ps + d,
+                   label=f"nq4 d={d} ps={ps} s={splits}")
+
+
 def test_mixed_lengths_many_splits(fa):
     lens = [2, 5000, 129, 8192, 7, 2048]
     _check(fa, lens, 4, 2, 128, 32, 0, seed=81, label="mixed auto")
