@@ -58,7 +58,7 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "profiling-recipe fallback"
 
 
-ATTN_KERNEL_FILES = ("attn_fwd.cuh", "attn_fwd_inst.cu", "attn_params.h", "ptx.cuh")
+ATTN_KERNEL_FILES = ("attn_fwd.cuh", "attn_fwd_inst.cu", "attn_params.h", "ptx.cuh", "sched.cuh")
 
 
 def kernel_source_hash(files=ATTN_KERNEL_FILES):
@@ -666,13 +666,10 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
 def rel_rmse_dev(a, ref):
     """RMSE(a - ref) / RMS(ref) over whole device tensors, accumulated in float64."""
     import torch
-    num = torch.zeros((), dtype=torch.float64, device=a.device)
-    den = torch.zeros((), dtype=torch.float64, device=a.device)
-    for x, r in zip(a.reshape(64, -1), ref.reshape(64, -1)):
-        r64 = r.double()
-        num += ((x.double() - r64) ** 2).sum()
-        den += (r64 ** 2).sum()
-    return float(torch.sqrt(num / den))
+    r64 = ref.double()
+    num = torch.linalg.vector_norm(a.double() - r64)
+    den = torch.linalg.vector_norm(r64)
+    return float(num / den)
 
 
 def run_profile_case(args):
