@@ -682,7 +682,7 @@ def run_profile_case(args):
     torch.cuda.set_device(0)
     b, h, n, d = 2, 16, 8192, 128       # 3 x 67 MB of Q/K/V: above L2 together
     if args.profile.startswith("quant"):
-        b = 8                           # one 537 MB tensor: above L2 on its own
+        b = 8                           # one 268 MB bf16 tensor: above L2 on its own
     q, k, v = make_qkv(b, h, n, d, seed=0, outliers=args.profile.startswith("fp8") or
                        args.profile.startswith("quant"))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
