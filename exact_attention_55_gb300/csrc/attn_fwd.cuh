@@ -545,13 +545,20 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             if (!unit_of<C>(su, p, w, tab)) continue;
             const int a = w.q0 + grp * C::BM;    // first row of this Q tile
             const int row = a + row_in_tile;     // this thread's query row
-            // keys allowed for this row: [jlo, jhi] (positions inside the sequence)
-            int jlo = 0, jhi = w.N - 1;
-            if (p.causal) jhi = min(jhi, row);
-            if (p.window > 0) {
-                jlo = row - p.window;
-                if (!p.causal) jhi = min(jhi, row + p.window);
-            }
+            // keys allowed for row r: [jlo(r), jhi(r)] (positions inside the sequence); both
+            // bounds grow with r, so this warp's 32 rows span jlo in [lo_min, lo_max] and jhi
+            // in [hi_min, hi_max], the bounds of its first and last row (warp-uniform)
+            auto key_bounds = [&](int r, int& lo, int& hi) {
+                lo = 0;
+                hi = w.N - 1;
+                if (p.causal) hi = min(hi, r);
+                if (p.window > 0) {
+                    lo = r - p.window;
+                    if (!p.causal) hi = min(hi, r + p.window);
+                }
+            };
+            int jlo, jhi;
+            key_bounds(row, jlo, jhi);
             // fp8: O is kept in units of the current key tile's V descale: before
             // P(t) V8(t) is added, O *= alpha * dv(t-1) / dv(t).  When every V block scale
             // is a power of two (v_pow2), O is kept in units of the largest V scale seen so
@@ -623,10 +630,22 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                                    (c0 < a + C::BM - 1 - p.window ||
                                     (!p.causal && c0 + C::BN - 1 > a + p.window)));
                 if (edge) {
+                    // per 32-key chunk, for this warp's rows: allowed for every row (skipped)
+                    // or not; key c0 + e is allowed iff c0 + e - jlo lies in [0, jhi - jlo],
+                    // and a chunk masked for every row takes an offset that fails every test
+                    int lo_min, hi_min, lo_max, hi_max;
+                    key_bounds(a + wq * 32, lo_min, hi_min);
+                    key_bounds(a + wq * 32 + 31, lo_max, hi_max);
+                    const uint32_t span = (uint32_t)(jhi - jlo);
 #pragma unroll
-                    for (int e = 0; e < C::BN; ++e) {
-                        const int j = c0 + e;
-                        if (j < jlo || j > jhi) s[e] = NEG_INF;
+                    for (int ch = 0; ch < C::BN / 32; ++ch) {
+                        const int x0 = c0 + ch * 32, x1 = x0 + 31;
+                        if (!(x0 >= lo_max && x1 <= hi_min)) {
+                            const int base = (x1 < lo_min || x0 > hi_max) ? -(1 << 30) : x0 - jlo;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if ((uint32_t)(base + e) > span) s[ch * 32 + e] = NEG_INF;
+                        }
                     }
                 }
                 // row max: 8 independent chains of 3-input maxima, then a small tree
