@@ -61,12 +61,12 @@ __host__ __device__ constexpr int quant_smem_bytes(int d)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// RN(x / s) for s > 0 finite and a normal quotient, from y = RN(1/s).
-__device__ __forceinline__ float div_by_scale(float x, float s, float y)
+// Per half: the larger of two bf16 values (a NaN loses to the other operand, as in fmaxf).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b)
 {
-    const float q = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q, s, x);
-    return (r == 0.0f) ? q : __fmaf_rn(r, y, q);
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
@@ -78,7 +78,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// RN(x / s) for two values at once (the same three roundings as div_by_scale).
+// RN(x / s) for two values at once, s > 0 finite and the quotients normal, from
+// y = RN(1/s) and s_neg = -s: q = RN(x y), r = x - q s (exact), RN(q + r y).
 __device__ __forceinline__ float2 div2_by_scale(float2 x, float2 s_neg, float2 y)
 {
     const float2 q = __fmul2_rn(x, y);
@@ -189,20 +190,21 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
         float scale;
         if constexpr (DR == 0) {
             const int nchunk = block_rows(blk) * p.d / 8;  // 16-byte chunks of 8 bf16
-            float amax = 0.0f;
+            // amax on packed bf16 pairs: |x| is x with the sign bit cleared, and the
+            // maximum of bf16 values is exact (NaN ignored, as by fmaxf)
+            uint32_t mag2 = 0;
             for (int g = threadIdx.x; g < nchunk; g += kThreads) {
                 const uint4 v = *reinterpret_cast<const uint4*>(st + g * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    amax = fmax3(amax, fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e])));
+                mag2 = max_bf16x2(mag2, max_bf16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+                mag2 = max_bf16x2(mag2, max_bf16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
             }
-            amax = block_amax(amax);
+            const float amax = block_amax(fmaxf(bf16_lo(mag2), bf16_hi(mag2)));
             scale = (amax > 0.0f) ? __fdiv_rn(amax, FMT == 1 ? 57344.0f : 448.0f) : 1.0f;
             if (FMT == 2 && amax > 0.0f) scale = pow2_at_least(scale);
             const float y = __frcp_rn(scale);
-            auto pack2 = [](float lo, float hi) -> uint32_t {
-                return FMT == 1 ? pack_e5m2x2(lo, hi) : pack_e4m3x2(lo, hi);
+            const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
+            auto pack2 = [](float2 t) -> uint32_t {
+                return FMT == 1 ? pack_e5m2x2(t.x, t.y) : pack_e4m3x2(t.x, t.y);
             };
 
             uint2* dst = reinterpret_cast<uint2*>(p.x8 + block_base(blk));
@@ -212,11 +214,10 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 uint32_t out[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const uint32_t lo = pack2(div_by_scale(bf16_lo(w[2 * e]), scale, y),
-                                              div_by_scale(bf16_hi(w[2 * e]), scale, y));
-                    const uint32_t hi = pack2(div_by_scale(bf16_lo(w[2 * e + 1]), scale, y),
-                                              div_by_scale(bf16_hi(w[2 * e + 1]), scale, y));
-                    out[e] = lo | (hi << 16);
+                    const float2 a = div2_by_scale(make_float2(bf16_lo(w[2 * e]), bf16_hi(w[2 * e])), sn2, y2);
+                    const float2 b = div2_by_scale(make_float2(bf16_lo(w[2 * e + 1]), bf16_hi(w[2 * e + 1])),
+                                                   sn2, y2);
+                    out[e] = pack2(a) | (pack2(b) << 16);
                 }
                 __stcs(dst + g, make_uint2(out[0], out[1]));
             }
