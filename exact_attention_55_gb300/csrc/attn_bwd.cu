@@ -123,10 +123,19 @@ struct BwdUnit {
     int N;            // rows of the sequence
     int c1, c2;       // TMA coordinates of row 0: (row offset, head) or (head, token)
     bool packed;
-    size_t vbase;     // LSE / D index of row 0
-    size_t obase;     // output row index of row 0
-    int ostride;      // output rows between consecutive sequence rows
 };
+
+// LSE / D index of row r of the unit's sequence: batched [BH, N]; packed [H, T].
+__device__ __forceinline__ size_t bwd_vidx(const BwdParams& p, const BwdUnit& u, int r)
+{
+    return u.packed ? (size_t)u.c1 * p.T + (size_t)(u.c2 + r) : (size_t)u.c2 * p.N + r;
+}
+
+// Output row (of d elements) of row r: batched [BH, N, d]; packed [T, H, d].
+__device__ __forceinline__ size_t bwd_orow(const BwdParams& p, const BwdUnit& u, int r)
+{
+    return u.packed ? (size_t)(u.c2 + r) * p.H + u.c1 : (size_t)u.c2 * p.N + r;
+}
 
 __device__ __forceinline__ void bwd_coords(const BwdUnit& u, int r, int& c1, int& c2)
 {
@@ -195,9 +204,6 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u, 
         u.N = p.N;
         u.c1 = 0;
         u.c2 = sh;
-        u.vbase = (size_t)sh * p.N;
-        u.obase = (size_t)sh * p.N;
-        u.ostride = 1;
     } else {
         const int seq = sh / p.H, h = sh - seq * p.H;
         const int a = min(max(__ldg(p.cu_seqlens + seq), 0), p.T);
@@ -205,9 +211,6 @@ __device__ __forceinline__ bool bwd_unit(const BwdParams& p, int s, BwdUnit& u, 
         u.N = b - a;
         u.c1 = h;
         u.c2 = a;
-        u.vbase = (size_t)h * p.T + a;
-        u.obase = (size_t)a * p.H + h;
-        u.ostride = p.H;
     }
     const int nt = (u.N + 127) / 128;
     if (k >= ((nt + 1) >> 1)) return false;      // beyond this sequence's pairs (or empty)
@@ -607,7 +610,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
         float* my_lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512) + warp * 128;
         float* my_delta = my_lse2 + 64;
         auto col_load = [&](const BwdUnit& cu, int c, float2& l2v, float2& dv) {
-            const size_t base = cu.vbase;
+            const size_t base = bwd_vidx(p, cu, 0);
             const int c0 = min(c + 2 * lane, cu.N - 1), c1 = min(c + 2 * lane + 1, cu.N - 1);
             l2v = make_float2(__ldg(p.lse + base + c0) * LOG2E, __ldg(p.lse + base + c1) * LOG2E);
             dv = make_float2(__ldg(p.delta + base + c0), __ldg(p.delta + base + c1));
@@ -622,8 +625,8 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
             const bool valid = my < NS;
             float lse2 = 0.0f, dlt = 0.0f;              // dQ pass: per-row LSE and D
             if constexpr (kDQ) {
-                lse2 = valid ? p.lse[un.vbase + my] * LOG2E : 0.0f;
-                dlt = valid ? p.delta[un.vbase + my] : 0.0f;
+                lse2 = valid ? p.lse[bwd_vidx(p, un, my)] * LOG2E : 0.0f;
+                dlt = valid ? p.delta[bwd_vidx(p, un, my)] : 0.0f;
             }
             // The columns (the other index) the mask allows for this thread's row form one
             // interval [m_lo, m_hi]: for a query row, keys from i - w (w > 0) or 0 to i
@@ -806,7 +809,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kDQ>::NUM_THREADS, 1)
                 const int which = kDQ ? 0 : wg;
                 const float f = kDQ ? p.scale : (which == 0 ? 1.0f : p.scale);
                 __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(kDQ ? p.dq : (which == 0 ? p.dv : p.dk));
-                out += (un.obase + (size_t)my * un.ostride) * D;
+                out += bwd_orow(p, un, my) * D;
                 constexpr int NCH = kDQ ? D / 64 : D / 32;     // 32-column chunks per warpgroup
                 const int ch0 = kDQ ? wg * NCH : 0;
 #pragma unroll

@@ -51,6 +51,20 @@ def test_multi_tile_ragged(fa, d, causal, window):
     _full_check(fa, q, k, v, 1.0 / math.sqrt(d), causal, window, f"d={d} c={causal} w={window}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("window", [1, 31, 32, 33, 127, 129])
+def test_narrow_windows(fa, d, window):
+    """Windows around the 32-key chunk and the 128-key tile: the edge tiles' chunks are
+    allowed for every row of a warp, masked for every row, or mixed, in every combination;
+    N = 600 leaves a ragged last tile.  V is scaled by 1/4 (exact in bf16): with a window of
+    a few keys O is nearly one V row, and the absolute bf16 bars assume O averages many rows;
+    a masking error still moves O by the size of a V row."""
+    q, k, v = make_qkv(1, 2, 600, d, seed=40 + window)
+    v = v * 0.25
+    for causal in (False, True):
+        _full_check(fa, q, k, v, 1.0 / math.sqrt(d), causal, window, f"d={d} w={window} c={causal}")
+
+
 @pytest.mark.parametrize("N", [1, 7, 129, 255, 257, 513])
 def test_small_and_odd_lengths(fa, N):
     q, k, v = make_qkv(1, 3, N, 128, seed=N)

@@ -140,14 +140,22 @@ def test_fp8_attention_small(fa, causal, window):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_attention_d256(fa, causal):
+    """d = 256 on the FP8 workload's distribution at N = 512 (measured 0.73 % non-causal,
+    1.03 % causal over all rows: a causal row i averages P's E4M3 rounding over only i + 1
+    keys), so the bound here is that rounding's RMS."""
     e = _fp8_case(fa, 1, 2, 512, 256, causal, 0, seed=32)
+    print(f"fp8 d256 causal={causal}:", e)
     assert e["vs_deq"] <= FP8_P_ROUNDING_BOUND, e
     assert e["vs_unq"] <= e["oracle_deq_vs_unq"] + FP8_P_ROUNDING_BOUND, e
+    assert e["lse_bound_ratio"] <= 1.0, e
 
 
 def test_fp8_attention_without_outliers(fa):
-    """Spread attention (no outliers): P's E4M3 rounding dominates the error."""
+    """Spread attention (no outliers, not one of the FP8 workload's cases): O averages many
+    V rows and is small, so P's E4M3 rounding (up to 2^-4 relative per element) shows in the
+    relative error almost undiminished; the bound is that rounding's RMS."""
     e = _fp8_case(fa, 1, 4, 1024, 128, False, 0, seed=33, outliers=False)
+    print("fp8 without outliers:", e)
     assert e["vs_deq"] <= FP8_P_ROUNDING_BOUND, e
 
 
