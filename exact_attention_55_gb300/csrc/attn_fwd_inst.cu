@@ -16,7 +16,7 @@ namespace gb300 {
 
 template <int D, bool F8>
 cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                            const FwdParams& p, int sm_count, cudaStream_t stream)
+                            const CUtensorMap& tmO, const FwdParams& p, int sm_count, cudaStream_t stream)
 {
     using C = FwdCfg<D, F8>;
     // packed variable-length sequences run their own instantiation (bf16 only), so the
@@ -40,12 +40,12 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
         if (attr.numRegs * C::NUM_THREADS < C::REG_POOL) return cudaErrorInvalidConfiguration;
     }
     const int grid = p.num_units < sm_count ? p.num_units : sm_count;
-    kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
+    kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, p);
     return cudaGetLastError();
 }
 
 template cudaError_t launch_attn_fwd<GB300_ATTN_D, (GB300_ATTN_F8 != 0)>(
-    const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const FwdParams&, int,
-    cudaStream_t);
+    const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const FwdParams&,
+    int, cudaStream_t);
 
 }  // namespace gb300
