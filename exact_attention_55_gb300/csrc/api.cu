@@ -137,11 +137,6 @@ bool encode_3d_packed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
     return r == CUDA_SUCCESS;
 }
 
-// O tiles leave by TMA stores from a staging tile, except under a causal mask over
-// sequences shorter than 4096: there the softmax threads' own stores measured 4-8 %
-// faster (N <= 2048), even at 4096, and staging 2.5-4 % faster from 8192.
-int stage_o_tiles(int causal, int n) { return (causal && n < 4096) ? 0 : 1; }
-
 template <int D>
 attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                              const int* cu_seqlens, int num_seqs, int max_seqlen, int T, int H,
@@ -156,7 +151,7 @@ attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* 
     if (!encode_3d_packed(&mq, q, dt, C::EB, D, H, T, C::BM) ||
         !encode_3d_packed(&mk, k, dt, C::EB, D, H, T, C::BN) ||
         !encode_3d_packed(&mv, v, dt, C::EB, D, H, T, C::BN) ||
-        !encode_3d_packed(&mo, o, dt, 2, D, H, T, C::BM))  // O tiles leave by TMA stores
+        !encode_3d_packed(&mo, o, dt, 2, D, H, T, 32))  // O leaves by TMA stores of 32-row boxes
         return ATTN_ERR_CUDA;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -177,7 +172,6 @@ attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* 
     p.num_seqs = num_seqs;
     p.H = H;
     p.T = T;
-    p.stage_o = stage_o_tiles(p.causal, max_seqlen);
     if (launch_attn_fwd<D, false>(mq, mk, mv, mo, p, dev->sm_count, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
@@ -200,8 +194,8 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     if (!encode_3d(&mq, q, dt, C::EB, D, N, BH, C::BM, C::SWZ) ||
         !encode_3d(&mk, k, dt, C::EB, D, N, BH, C::BN, C::SWZ) ||
         !encode_3d(&mv, v, dt, C::EB, D, N, BH, C::BN, C::SWZ) ||
-        // O is bf16 in both paths and leaves by TMA stores of 64-column boxes
-        !encode_3d(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, C::BM, 128))
+        // O is bf16 in both paths and leaves by TMA stores of 64-column x 32-row boxes
+        !encode_3d(&mo, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, N, BH, 32, 128))
         return ATTN_ERR_CUDA;
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -225,7 +219,6 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.qk_fmt = qk_fmt;
     p.v_pow2 = v_pow2;
     p.qk_shift = qk_block == 64 ? 6 : 7;
-    p.stage_o = stage_o_tiles(p.causal, N);
     if (launch_attn_fwd<D, F8>(mq, mk, mv, mo, p, dev->sm_count, stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;

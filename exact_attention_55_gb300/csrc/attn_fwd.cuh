@@ -24,11 +24,10 @@
 //     apply the mask on edge tiles, update the running max with a lazy
 //     threshold, exponentiate with ex2, keep the running sum, write P to TMEM
 //     and, only when the stale maximum would let P exceed 2^tau, rescale their
-//     O rows in TMEM; at the end they normalise O, write the LSE and (bf16, d = 128)
-//     put the O tile into a shared-memory staging tile, from which
-//   * warp STORE (one lane) writes it to global memory with TMA stores while the
-//     softmax warps go on to the next unit (bf16 at d = 128; the other kernels, short
-//     causal launches and packed tiles that run past their sequence store directly).
+//     O rows in TMEM; at the end they normalise O, write the LSE and (d = 128) send
+//     their O rows out through a small shared-memory slab per warp with TMA stores, so
+//     they go on to the next unit without waiting for global stores (d = 64 and 256,
+//     and packed rows that run past their sequence, store directly).
 //   With NQ = 2 the two Q tiles ping-pong: one group's softmax runs while the
 //   tensor core works on the other tile's GEMMs.  With NQ = 1 (d = 256) S is
 //   double-buffered so QK^T of the next block overlaps the current softmax.
@@ -63,14 +62,13 @@ struct FwdCfg {
     // barriers (FwdBars, 256 bytes at most) followed by the packed-sequence schedule table
     static constexpr int BAR_BYTES = 2048;
     static constexpr int ALIGN_SLACK = 1024;
-    // bf16, d = 128: O leaves through a staging tile in shared memory (128 rows x d bf16, in
-    // 128-byte-swizzled blocks of 64 columns, the layout a TMA store reads) and TMA stores
-    // issued by the store warp, so the softmax warps do not wait on global stores.  (The
-    // fp8 and d = 64 kernels, bound by their softmax, measured 3-4 % slower with it.)
-    static constexpr bool OSTAGE = D == 128 && !F8;
-    static constexpr int O_CB_BYTES = BM * 128;          // one 64-column block of O rows
-    static constexpr int O_NCB = D * 2 / 128;
-    static constexpr int OSTAGE_BYTES = OSTAGE ? O_NCB * O_CB_BYTES : 0;
+    // d = 128: each softmax warp's 32 O rows leave through its own 4 KB slab of shared memory
+    // (32 rows x 64 bf16, 128-byte swizzled, the layout a TMA store reads), one 64-column half
+    // at a time, by TMA stores its lane 0 issues; the warp waits only for its own previous
+    // store.  (d = 64 measured 1 % slower with it; d = 256 has no shared memory to spare.)
+    static constexpr bool OSTAGE = D == 128;
+    static constexpr int O_SLAB_BYTES = 32 * 128;
+    static constexpr int OSTAGE_BYTES = OSTAGE ? 4 * NQ * O_SLAB_BYTES : 0;
     static constexpr int NSLOT_FIT =
         (SMEM_CAP - BAR_BYTES - ALIGN_SLACK - NQ * Q_BYTES - OSTAGE_BYTES) / KV_BYTES;
     static constexpr int NSLOT = NSLOT_FIT < 8 ? NSLOT_FIT : 8;
@@ -84,7 +82,6 @@ struct FwdCfg {
     static constexpr int NUM_SOFTMAX_WARPS = 4 * NQ;
     static constexpr int PRODUCER_WARP = NUM_SOFTMAX_WARPS;   // first warp of the last warpgroup
     static constexpr int MMA_WARP = NUM_SOFTMAX_WARPS + 1;
-    static constexpr int STORE_WARP = NUM_SOFTMAX_WARPS + 2;  // O staging tile -> global (TMA)
     static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + 4);  // whole warpgroups
     // Register split (NQ = 2 only): softmax warpgroups grow, the control warpgroup
     // shrinks.  Needs REG_POOL <= registers per thread at launch * NUM_THREADS.
@@ -118,8 +115,6 @@ struct alignas(8) FwdBars {
     uint64_t p_full[2];
     uint64_t pv_done[2];
     uint64_t o_empty[2];
-    uint64_t ostage_full;   // the staging tile holds a Q tile's O (4 warps arrive)
-    uint64_t ostage_empty;  // its TMA store has read it (the store warp arrives)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -240,19 +235,17 @@ __device__ __forceinline__ void tile_steps(const Unit& w, int i, const FwdParams
     }
 }
 
-// Whether Q tile i of unit w leaves through the staging tile and a TMA store (when the
-// launch asks for it): batched rows past N are clipped by the tensor map; a packed tile
-// that runs past its sequence's end would write into the next sequence, so such a tile
-// (and any tile of d = 256) is stored directly by the softmax warps.  Every role
-// evaluates the same condition.
+// Whether the 32 O rows of softmax warp wq of the Q tile starting at row a leave through the
+// warp's slab and TMA stores: batched rows past N are clipped by the tensor map; packed rows
+// that run past their sequence's end would write into the next sequence, so such a warp (and
+// every warp at d = 64 or 256) stores its rows directly.
 template <class C>
-__device__ __forceinline__ bool tile_staged(const Unit& w, int i, const FwdParams& p)
+__device__ __forceinline__ bool slab_staged(const Unit& w, int a, int wq)
 {
     if constexpr (!C::OSTAGE) return false;
-    if (!p.stage_o) return false;
-    const int a = w.q0 + i * C::BM;
-    if (a >= w.N) return false;
-    if constexpr (C::PACKED) return a + C::BM <= w.N;
+    const int r0 = a + wq * 32;
+    if (r0 >= w.N) return false;
+    if constexpr (C::PACKED) return r0 + 32 <= w.N;
     return true;
 }
 
@@ -274,7 +267,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                                                ~uintptr_t(1023));
     uint8_t* q_smem = smem;                                   // NQ tiles
     uint8_t* kv_smem = smem + C::NQ * C::Q_BYTES;             // NSLOT tiles
-    uint8_t* ostage = kv_smem + C::NSLOT * C::KV_BYTES;       // O staging tile (bf16, d = 128)
+    uint8_t* ostage = kv_smem + C::NSLOT * C::KV_BYTES;       // O slabs, one per softmax warp
     FwdBars* bars = reinterpret_cast<FwdBars*>(ostage + C::OSTAGE_BYTES);
     const volatile int* abort_flag = &bars->abort_flag;
 
@@ -304,8 +297,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             mbar_init(smem_u32(&bars->kv_full[s]), 1);
             mbar_init(smem_u32(&bars->kv_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars->ostage_full), 4);
-        mbar_init(smem_u32(&bars->ostage_empty), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -568,7 +559,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
         const float NEG_INF = -__int_as_float(0x7f800000);
         uint32_t s_phase = 0, pv_phase = 0;  // per-buffer / per-tile parities
         uint32_t uc = 0;
-        uint32_t kst = 0;  // staged Q tiles of both groups so far (the staging tile's uses)
         bool ok = true;
 
         auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -827,13 +817,12 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
             if constexpr (F8) inv_l *= dv_cur * (1.0f / float(1u << C::P8_SHIFT));
             const uint32_t o_addr = tmem + lane_addr + C::O_COL0 + grp * D;
-            const bool st0 = tile_staged<C>(w, 0, p);
-            const bool st1 = (C::NQ == 2) && tile_staged<C>(w, 1, p);
-            if (grp == 0 ? st0 : st1) {
-                // O's row as bf16 pairs in registers, TMEM released, then the row into the
-                // staging tile (row r's 16-byte chunk c of column block b at b * 16 KB +
-                // r * 128 + ((c ^ (r & 7)) * 16): the 128-byte swizzle the tensor map uses)
-                // once the tile's previous store has read it; the store warp writes it out
+            if (slab_staged<C>(w, a, wq)) {
+                // O's row as bf16 pairs in registers, TMEM released, then the warp's 32 rows
+                // leave in 64-column halves through its own 4 KB slab of the staging area
+                // (row r's 16-byte chunk c at r * 128 + ((c ^ (r & 7)) * 16): the 128-byte
+                // swizzle of the tensor map): lane 0 waits until its previous store has read
+                // the slab, the lanes write it, lane 0 issues the TMA store
                 uint32_t pk[D / 2];
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch) {
@@ -848,17 +837,27 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[grp]));
-                const uint32_t item = kst + ((grp == 1 && st0) ? 1u : 0u);
-                if (!wait_all(&bars->ostage_empty, (item & 1) ^ 1)) break;
-                const int r = row_in_tile;
+                uint8_t* slab = ostage + warp * C::O_SLAB_BYTES;
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    uint8_t* dst = ostage + (c >> 3) * C::O_CB_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                for (int hc = 0; hc < D / 64; ++hc) {
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(slab + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[hc * 32 + 4 * c], pk[hc * 32 + 4 * c + 1], pk[hc * 32 + 4 * c + 2],
+                                       pk[hc * 32 + 4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int r0 = a + wq * 32;
+                        if constexpr (!C::PACKED)  // map (d, N, BH)
+                            tma_store_3d(&tmO, smem_u32(slab), hc * 64, r0, w.z);
+                        else                       // map (d, H, T)
+                            tma_store_3d(&tmO, smem_u32(slab), hc * 64, w.z, w.y0 + r0);
+                        bulk_commit_group();
+                    }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->ostage_full));
             } else {
                 // batched: o[z][row]; packed: o[y0 + row][z] ([T, H, D])
                 const size_t orow_idx = (!C::PACKED)
@@ -886,7 +885,6 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->o_empty[grp]));
             }
-            kst += (st0 ? 1u : 0u) + (st1 ? 1u : 0u);
             if (row < w.N) {
                 const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : NEG_INF;
                 const size_t li = (!C::PACKED) ? (size_t)w.z * p.N + row
@@ -897,47 +895,13 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
         }
         if (!ok) raise_timeout(p, bars);
         tmem_wait_st();  // an aborted step may have left a P or O store in flight
-    } else {
-        // ------------------------------------------------------------ store warp, spares
-        if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
         if constexpr (C::OSTAGE) {
-            if (warp == C::STORE_WARP) {
-                // The staging tile to global memory, in the order the softmax groups fill
-                // it (Q tile 0, then 1, of each unit): lane 0 issues one TMA store per
-                // 64-column block and frees the tile once the stores have read it.
-                uint32_t k = 0;  // staged tiles so far
-                bool ok = true;
-                for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
-                    Unit w;
-                    if (!unit_of<C>(su, p, w, tab)) continue;
-                    for (int i = 0; i < C::NQ; ++i) {
-                        if (!tile_staged<C>(w, i, p)) continue;
-                        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->ostage_full), k & 1,
-                                                               abort_flag, p.timeout_ns));
-                        if (!ok) break;
-                        if (lane == 0) {
-                            const int row = w.q0 + i * C::BM;
-#pragma unroll
-                            for (int cb = 0; cb < C::O_NCB; ++cb) {
-                                const uint32_t src = smem_u32(ostage + cb * C::O_CB_BYTES);
-                                if constexpr (!C::PACKED)  // map (d, N, BH)
-                                    tma_store_3d(&tmO, src, cb * 64, row, w.z);
-                                else                       // map (d, H, T)
-                                    tma_store_3d(&tmO, src, cb * 64, w.z, w.y0 + row);
-                            }
-                            bulk_commit_group();
-                            bulk_wait_group_read0();
-                            mbar_arrive(smem_u32(&bars->ostage_empty));
-                        }
-                        __syncwarp();
-                        ++k;
-                    }
-                }
-                if (!ok && lane == 0) raise_timeout(p, bars);
-                if (lane == 0) bulk_wait_group0();  // every store has landed before the CTA ends
-                __syncwarp();
-            }
+            if (lane == 0) bulk_wait_group0();  // this warp's O stores have landed
+            __syncwarp();
         }
+    } else {
+        // ------------------------------------------------------------ spare warps
+        if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CONTROL>();
     }
 
     tc_fence_before_sync();

@@ -40,8 +40,6 @@ struct FwdParams {
     int qk_fmt;           // fp8 path: format of the Q and K codes, 0 E4M3, 1 E5M2 (V is E4M3)
     int v_pow2;           // fp8 path: V's block scales are powers of two (see the softmax)
     int qk_shift;         // fp8 path: log2 of the rows per Q and K scale block, 6 or 7 (V: 128)
-    int stage_o;          // 1: finished O tiles leave by TMA stores from a staging tile (bf16, d = 128);
-                          // 0: the softmax threads store them (faster for short causal sequences)
     // Packed variable-length sequences (null cu_seqlens: the batched [BH, N, D] layout).
     // q, k, v, o are [T, H, D]; lse is [H, T]; sequence s is tokens [cu[s], cu[s+1]).
     // Units are (sequence, head, pair of query blocks) with num_qblk from max_seqlen.
