@@ -450,7 +450,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
-// Pack two floats into e4m3x2 (round to nearest even, saturate to +-448): `lo` in bits 0-7.
+// Pack two floats into e5m2x2 (round to nearest even, saturate to +-57344): `lo` in bits 0-7.
 __device__ __forceinline__ uint16_t pack_e5m2x2(float lo, float hi)
 {
     uint16_t r;
@@ -458,6 +458,7 @@ __device__ __forceinline__ uint16_t pack_e5m2x2(float lo, float hi)
     return r;
 }
 
+// Pack two floats into e4m3x2 (round to nearest even, saturate to +-448): `lo` in bits 0-7.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi)
 {
     uint16_t r;
