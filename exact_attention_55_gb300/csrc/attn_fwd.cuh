@@ -142,7 +142,11 @@ struct Unit {
 // balance is built into the order).  Pairs of one head are adjacent, so CTAs that
 // run at the same time share that head's K/V in L2.  Sub-unit s is half (s & 1)
 // of pair s >> 1, the heavy half first; a CTA walks 2c, 2c+1, 2c+2G, 2c+2G+1, ...
-// Returns false for the empty second half of the middle pair when nq is odd.
+// Without a causal mask the units of a head cost the same (with a window, all but the
+// few near the sequence's ends), and when whole pairs would leave part of the grid a
+// round short (512 pairs on 152 CTAs: 4 rounds for some, 3 for the rest) a CTA walks
+// single units c, c+G, c+2G, ... instead (unit_walk, chosen by the host).  Returns
+// false for the empty second half of the middle pair when nq is odd.
 // Packed sequences ("FlashAttention V3：优化框架吞吐量的关键技术实践" §1.1, variable
 // sequence lengths): pair slots are laid out for the longest sequence and a
 // shorter one skips the slots it does not have; offsets are clamped to [0, T] so
@@ -203,6 +207,21 @@ __device__ __forceinline__ int next_sub(int s, const SortTab* tab)
 {
     if (tab == nullptr || !(s & 1)) return next_sub(s);
     return snake_next_sub(s);
+}
+
+// This CTA's first sub-unit and its next one after s: packed sequences walk pairs (round-
+// robin or snake); the batched kernel takes the strides the launch wrote for its grid.
+template <class C>
+__device__ __forceinline__ int first_sub(const FwdParams& p)
+{
+    if constexpr (C::PACKED) return 2 * (int)blockIdx.x;
+    else return (int)blockIdx.x * p.walk_first;
+}
+template <class C>
+__device__ __forceinline__ int next_sub(int s, const FwdParams& p, const SortTab* tab)
+{
+    if constexpr (C::PACKED) return next_sub(s, tab);
+    else return s + ((s & 1) ? p.walk_odd : p.walk_even);
 }
 
 // Sub-units [0, 2 * pairs) exist: pair slots of the layout, or the table's exact count.
@@ -324,7 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             uint32_t ring = 0, uc = 0;
             uint32_t q_armed[2] = {0, 0};
             bool ok = true;
-            for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
+            for (int su = first_sub<C>(p); su < num_subs(p, tab) && ok; su = next_sub<C>(su, p, tab)) {
                 Unit w;
                 if (!unit_of<C>(su, p, w, tab)) continue;
                 for (int i = 0; i < C::NQ && ok; ++i) {
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             }
         };
 
-        for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
+        for (int su = first_sub<C>(p); su < num_subs(p, tab) && ok; su = next_sub<C>(su, p, tab)) {
             Unit w;
             if (!unit_of<C>(su, p, w, tab)) continue;
 #pragma unroll
@@ -568,7 +587,7 @@ __global__ void __launch_bounds__(FwdCfg<D, F8>::NUM_THREADS, 1)
             return r;
         };
 
-        for (int su = 2 * blockIdx.x; su < num_subs(p, tab) && ok; su = next_sub(su, tab)) {
+        for (int su = first_sub<C>(p); su < num_subs(p, tab) && ok; su = next_sub<C>(su, p, tab)) {
             Unit w;
             if (!unit_of<C>(su, p, w, tab)) continue;
             const int a = w.q0 + grp * C::BM;    // first row of this Q tile

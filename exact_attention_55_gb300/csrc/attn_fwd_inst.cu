@@ -39,8 +39,13 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
         if (e != cudaSuccess) return e;
         if (attr.numRegs * C::NUM_THREADS < C::REG_POOL) return cudaErrorInvalidConfiguration;
     }
-    const int grid = p.num_units < sm_count ? p.num_units : sm_count;
-    kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, p);
+    const int subs = p.unit_walk ? 2 * p.num_units : p.num_units;  // what the CTAs stride over
+    const int grid = subs < sm_count ? subs : sm_count;
+    FwdParams q = p;
+    q.walk_first = p.unit_walk ? 1 : 2;
+    q.walk_even = p.unit_walk ? grid : 1;
+    q.walk_odd = p.unit_walk ? grid : 2 * grid - 1;
+    kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,12 @@ struct FwdParams {
     int N;                // sequence length (queries = keys)
     int num_qblk;         // query blocks per head (NQ * 128 rows each)
     int num_units;        // BH * ceil(num_qblk / 2): pairs of query blocks
+    int unit_walk;        // 1: each CTA strides over single units (batched, non-causal or
+                          // windowed, when that takes fewer rounds); 0: over whole pairs
+    int walk_first;       // batched walk, set at launch for its grid G: CTA c starts at
+    int walk_even;        // sub-unit c * walk_first and steps by walk_even from an even
+    int walk_odd;         // sub-unit, walk_odd from an odd one (pairs: 2, 1, 2G - 1;
+                          // single units: 1, G, G)
     int causal;           // 1: key j allowed only for j <= i
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
