@@ -137,25 +137,25 @@ bool encode_3d_packed(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
     return r == CUDA_SUCCESS;
 }
 
-// Whether the batched forward's CTAs stride over single units instead of complementary
-// pairs.  Pairs balance a causal mask.  Without one the units of a head cost the same,
-// and a walk over single units ends in fewer rounds whenever whole pairs leave part of
-// the grid a round short (for example 512 pairs on 152 SMs: 4 pair rounds = 8 unit
-// times, against 7 unit rounds).  With a window, the units within a window of the
-// sequence's start (causal) or of either end are lighter; with 152 CTAs (a multiple of
-// 8) a plain stride hands each CTA the same position in every head, so single units are
-// taken only when those edge units are at most 1/16 of a head's (measured: w = 1024 at
-// N = 16384 gains 8 %, at N = 2048 loses 9 %).
+// How the batched forward's CTAs walk the work: 0 complementary pairs, 1 single units
+// with a plain stride, 2 single units in rotated rounds.  Pairs balance a causal mask.  Without one the units of a head cost
+// the same, and single units end in fewer rounds whenever whole pairs leave part of the
+// grid a round short (for example 512 pairs on 152 SMs: 4 pair rounds = 8 unit times,
+// against 7 unit rounds).  With a window the units within a window of the sequence's
+// ends are lighter; pairs then land on the same positions of every head round after
+// round (152 is a multiple of 4 and 8), while the rotated rounds move each CTA along a
+// head's units, so a window takes rotated single units unless they need more rounds.
+// (Without a window the plain stride measured slightly faster than the rotated one.)  A
+// window of N - 1 keys or more masks nothing beyond the causal mask (or nothing at all),
+// and is walked as that mask is (for a causal one, complementary pairs balance exactly).
 int single_unit_walk(int causal, int window, int N, long long pairs, int sm_count)
 {
+    if (window >= N - 1) window = 0;
     if (causal && window <= 0) return 0;
-    if (window > 0) {
-        const long long edge = causal ? (long long)window : 2LL * window;
-        if (edge * 16 > (long long)N) return 0;
-    }
     const long long G = sm_count > 0 ? sm_count : 1;
     const long long pair_times = 2 * ((pairs + G - 1) / G);   // in units of one unit's time
     const long long unit_times = (2 * pairs + G - 1) / G;
+    if (window > 0) return unit_times <= pair_times ? 2 : 0;
     return unit_times < pair_times ? 1 : 0;
 }
 
@@ -184,7 +184,8 @@ attn_status_t run_fwd_varlen(const void* q, const void* k, const void* v, void* 
     p.N = max_seqlen;
     p.num_qblk = (max_seqlen + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     const long long units = (long long)num_seqs * H * ((p.num_qblk + 1) / 2);
-    if (2 * units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    // sub-unit indices, and a walk's step past the last one (< 4 * grid), stay in int
+    if (2 * units + 4LL * dev->sm_count > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     p.causal = causal ? 1 : 0;
     p.window = window > 0 ? window : 0;
@@ -231,7 +232,8 @@ attn_status_t run_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.N = N;
     p.num_qblk = (N + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     const long long units = (long long)BH * ((p.num_qblk + 1) / 2);
-    if (2 * units > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    // sub-unit indices, and a walk's step past the last one (< 4 * grid), stay in int
+    if (2 * units + 4LL * dev->sm_count > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     p.num_units = (int)units;
     p.unit_walk = single_unit_walk(causal, window, N, units, dev->sm_count);
     p.causal = causal ? 1 : 0;

@@ -142,11 +142,11 @@ struct Unit {
 // balance is built into the order).  Pairs of one head are adjacent, so CTAs that
 // run at the same time share that head's K/V in L2.  Sub-unit s is half (s & 1)
 // of pair s >> 1, the heavy half first; a CTA walks 2c, 2c+1, 2c+2G, 2c+2G+1, ...
-// Without a causal mask the units of a head cost the same (with a window, all but the
-// few near the sequence's ends), and when whole pairs would leave part of the grid a
-// round short (512 pairs on 152 CTAs: 4 rounds for some, 3 for the rest) a CTA walks
-// single units c, c+G, c+2G, ... instead (unit_walk, chosen by the host).  Returns
-// false for the empty second half of the middle pair when nq is odd.
+// Without a causal mask the units of a head cost the same (with a window, all but those
+// near the sequence's ends), and when whole pairs would leave part of the grid a round
+// short (512 pairs on 152 CTAs: 4 rounds for some, 3 for the rest) the CTAs walk single
+// units in rotated rounds instead (unit_walk, chosen by the host; see first_sub).
+// Returns false for the empty second half of the middle pair when nq is odd.
 // Packed sequences ("FlashAttention V3：优化框架吞吐量的关键技术实践" §1.1, variable
 // sequence lengths): pair slots are laid out for the longest sequence and a
 // shorter one skips the slots it does not have; offsets are clamped to [0, T] so
@@ -210,7 +210,15 @@ __device__ __forceinline__ int next_sub(int s, const SortTab* tab)
 }
 
 // This CTA's first sub-unit and its next one after s: packed sequences walk pairs (round-
-// robin or snake); the batched kernel takes the strides the launch wrote for its grid.
+// robin or snake); batched launches walk pairs round-robin, or single units with a plain
+// stride (no mask: every unit costs the same), or under a window single units in rotated
+// rounds: in round r CTA c takes unit r*G + (c + r) mod G.  Each round covers the same
+// G units as a plain stride, but a CTA moves one position along a head's units per
+// round; with a plain stride and G a multiple of a head's unit count, every CTA would
+// meet the same position (under a window, the same cost) in every head.
+// The batched walks are one rule whose constants the launch writes: pairs step +1 from
+// the first half to the second and +(2G - 1) to the next pair; plain-stride units +G;
+// rotated units +(G + 1), or +1 where (c + r + 1) mod G wraps to 0.
 template <class C>
 __device__ __forceinline__ int first_sub(const FwdParams& p)
 {
@@ -221,7 +229,7 @@ template <class C>
 __device__ __forceinline__ int next_sub(int s, const FwdParams& p, const SortTab* tab)
 {
     if constexpr (C::PACKED) return next_sub(s, tab);
-    else return s + ((s & 1) ? p.walk_odd : p.walk_even);
+    else return s + 1 + (((s + p.walk_a) % p.walk_m == 0) ? 0 : p.walk_step);
 }
 
 // Sub-units [0, 2 * pairs) exist: pair slots of the layout, or the table's exact count.

@@ -42,9 +42,13 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
     const int subs = p.unit_walk ? 2 * p.num_units : p.num_units;  // what the CTAs stride over
     const int grid = subs < sm_count ? subs : sm_count;
     FwdParams q = p;
-    q.walk_first = p.unit_walk ? 1 : 2;
-    q.walk_even = p.unit_walk ? grid : 1;
-    q.walk_odd = p.unit_walk ? grid : 2 * grid - 1;
+    if (p.unit_walk == 0) {          // pairs: 2c, 2c + 1, 2c + 2G, 2c + 2G + 1, ...
+        q.walk_first = 2, q.walk_a = 0, q.walk_m = 2, q.walk_step = 2 * grid - 2;
+    } else if (p.unit_walk == 1) {   // single units, plain stride: c, c + G, ...
+        q.walk_first = 1, q.walk_a = 1, q.walk_m = 0x7fffffff, q.walk_step = grid - 1;
+    } else {                         // single units, rotated rounds
+        q.walk_first = 1, q.walk_a = 1, q.walk_m = grid, q.walk_step = grid;
+    }
     kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
     return cudaGetLastError();
 }

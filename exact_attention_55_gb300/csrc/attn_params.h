@@ -30,12 +30,14 @@ struct FwdParams {
     int N;                // sequence length (queries = keys)
     int num_qblk;         // query blocks per head (NQ * 128 rows each)
     int num_units;        // BH * ceil(num_qblk / 2): pairs of query blocks
-    int unit_walk;        // 1: each CTA strides over single units (batched, non-causal or
-                          // windowed, when that takes fewer rounds); 0: over whole pairs
-    int walk_first;       // batched walk, set at launch for its grid G: CTA c starts at
-    int walk_even;        // sub-unit c * walk_first and steps by walk_even from an even
-    int walk_odd;         // sub-unit, walk_odd from an odd one (pairs: 2, 1, 2G - 1;
-                          // single units: 1, G, G)
+    int unit_walk;        // batched walk, chosen by the host: 0 whole pairs, 1 single units
+                          // with a plain stride (non-causal), 2 single units in rotated
+                          // rounds (windowed)
+    int walk_first;       // the batched walk for the launch's grid G, set at launch: CTA c
+    int walk_a;           // starts at sub-unit c * walk_first, and after s goes to s + 1
+    int walk_m;           // when (s + walk_a) % walk_m == 0, else to s + 1 + walk_step
+    int walk_step;        // (pairs: 2, 0, 2, 2G - 2; plain stride: 1, 1, 2^31 - 1, G - 1;
+                          // rotated: 1, 1, G, G)
     int causal;           // 1: key j allowed only for j <= i
     int window;           // > 0: band of that half-width (left edge only when causal)
     float c_log2;         // softmax scale * log2(e)
