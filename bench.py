@@ -518,6 +518,20 @@ def measure_extra(fa, args, dev, stream, qd, kd, vd, q, k, v, scale, peaks):
                         "ms": statistics.mean(per), "shape": f"B1 H{hh} N16384 d{dd}",
                         "flops": "4 d per allowed (query, key) pair"}
         del qw, kw, vw, ow, lw
+    # a short band of the sweep (B8 H16 N2048 d128, causal, 1024-key window): half of each
+    # head's query blocks lie within a window of the start and cost less
+    qw, kw, vw = (t.to(dev) for t in make_qkv(8, 16, 2048, 128, seed=7))
+    ow = torch.empty_like(qw)
+    lw = torch.empty((8, 16, 2048), dtype=torch.float32, device=dev)
+    def band_step():
+        fa.attn_fwd_bf16(qw, kw, vw, scale=1.0 / math.sqrt(128), causal=True, window=1024,
+                         o=ow, lse=lw, stream=stream)
+    ms, per = time_steps(band_step, reps, 3, stream)
+    f = 4.0 * 128 * 8 * 16 * allowed_pairs(2048, True, 1024)
+    out["bf16_d128_n2048_causal_w1024"] = {"tflops": f / (statistics.mean(per) * 1e-3) / 1e12,
+                                           "ms": statistics.mean(per), "shape": "B8 H16 N2048 d128",
+                                           "flops": "4 d per allowed (query, key) pair"}
+    del qw, kw, vw, ow, lw
     # FP8 at head dim 64 with head-dim-aware scaling (Q, K per 64-row block, V per 128):
     # the FP8 workload's distribution at B16 H16 N8192 d64
     q6, k6, v6 = make_qkv(B, H, N, 64, seed=0, outliers=True)
