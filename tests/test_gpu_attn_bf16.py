@@ -150,6 +150,23 @@ def test_sweep(fa, d, N):
         assert torch.isfinite(o.float()).all()
 
 
+@pytest.mark.parametrize("d,H", [(128, 16), (256, 8)])
+def test_result_does_not_depend_on_the_walk(fa, d, H):
+    """B2 at N = 8192 has 512 query-block pairs, which the CTAs walk as single units; each
+    batch alone (256 pairs) is walked as pairs.  A unit's result depends only on its inputs,
+    so the two launches agree bit for bit."""
+    q, k, v = make_qkv(2, H, 8192, d, seed=11)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    scale = 1.0 / math.sqrt(d)
+    o2, l2 = fa.attn_fwd_bf16(qd, kd, vd, scale=scale)
+    for b in range(2):
+        o1, l1 = fa.attn_fwd_bf16(qd[b:b + 1].contiguous(), kd[b:b + 1].contiguous(),
+                                  vd[b:b + 1].contiguous(), scale=scale)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], o2[b]) and torch.equal(l1[0], l2[b])
+    assert fa.attn_get_device_status() == fa.ATTN_OK
+
+
 def test_repeated_calls_are_deterministic(fa):
     q, k, v = make_qkv(2, 4, 1024, 128, seed=9)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
