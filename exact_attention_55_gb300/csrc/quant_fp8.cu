@@ -100,11 +100,13 @@ __device__ __forceinline__ void butterfly2(float& a0, float& a1, float& b0, floa
     b0 = dif.x; b1 = dif.y;
 }
 
-// Launch shape per variant: 512 threads (four per row of a 128-row block); for the
-// rotated d <= 128 variants the registers are capped so two CTAs share an SM.
-// (Two threads per row -- one shuffle stage fewer, half the warps -- measured slower.)
+// Launch shape per variant: plain, 512 threads; rotated d = 64, one thread per row of a
+// 128-row block (all butterflies in registers, no shuffles); rotated d = 128 and 256, four
+// threads per row (one thread per row measured 12 % slower at d = 128, where 254 registers
+// a thread leave two 4-warp CTAs per SM; 24 % faster at d = 64).  Rotated d <= 128: two
+// or more CTAs per SM.
 template <int DR> struct QuantShape {
-    static constexpr int TPR = 4;
+    static constexpr int TPR = (DR == 64) ? 1 : 4;
     static constexpr int kThreads = (DR == 0) ? 512 : kQuantRows * TPR;
     static constexpr int kMinBlocks = (DR > 0 && DR <= 128) ? 2 : 1;
 };
@@ -224,17 +226,117 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
         } else {
             static_assert(DR == 64 || DR == 128 || DR == 256, "rotated head dim");
             constexpr int TPR = QuantShape<DR>::TPR;  // threads per row
+          if constexpr (TPR == 1) {
+            // One thread per row.  Register block b (8 elements) holds the row's 16-byte
+            // chunk b ^ z, z = r & 7: the eight rows of a quarter-warp then read eight
+            // different 16-byte slots of their 128-byte lines (rows 2 * DR bytes apart would
+            // otherwise hit the same banks).  The butterflies over chunk bits 0-2 (h = 8, 16,
+            // 32) pair register blocks b and b ^ 2^k whose chunks are swapped where bit k of
+            // z is set; there x' = fma(x, -1, y) = a - b and y' = fma(y, 1, x) = a + b land
+            // in the right chunks, each rounded once as in the sweep (sign sg = -1 for a
+            // swapped pair, +1 otherwise: x' = fma(x, sg, y), y' = fma(y, -sg, x)).
+            constexpr int NCH = DR / 8;               // chunks per row
+            const int r = threadIdx.x, z = r & 7;
+            const bool live = r < block_rows(blk);
+            float v[DR];
+#pragma unroll
+            for (int b = 0; b < NCH; ++b) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (b ^ z)) * 2);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * b + 2 * e] = bf16_lo(ww[e]);
+                    v[8 * b + 2 * e + 1] = bf16_hi(ww[e]);
+                }
+            }
+            // h = 1: neighbours inside a pair of registers
+#pragma unroll
+            for (int e = 0; e < DR; e += 2) {
+                const float a = v[e], bb = v[e + 1];
+                v[e] = __fadd_rn(a, bb);
+                v[e + 1] = __fsub_rn(a, bb);
+            }
+            // h = 2, 4: inside each chunk
+#pragma unroll
+            for (int h = 2; h < 8; h <<= 1)
+#pragma unroll
+                for (int b = 0; b < NCH; ++b)
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2)
+                        if (!(j & h)) butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * b + j + h], v[8 * b + j + h + 1]);
+            // h = 8, 16, 32: chunk bits 0-2, swapped per row by z
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const float sg = ((z >> k) & 1) ? -1.0f : 1.0f;
+                const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
+#pragma unroll
+                for (int b = 0; b < NCH; ++b) {
+                    if (b & (1 << k)) continue;
+                    const int b2 = b | (1 << k);
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        const float2 x = make_float2(v[8 * b + j], v[8 * b + j + 1]);
+                        const float2 y = make_float2(v[8 * b2 + j], v[8 * b2 + j + 1]);
+                        const float2 xn = __ffma2_rn(x, sg2, y);
+                        const float2 yn = __ffma2_rn(y, nsg2, x);
+                        v[8 * b + j] = xn.x; v[8 * b + j + 1] = xn.y;
+                        v[8 * b2 + j] = yn.x; v[8 * b2 + j + 1] = yn.y;
+                    }
+                }
+            }
+            // h = 64 (d = 128): chunk bit 3, not swapped
+#pragma unroll
+            for (int hm = 8; hm < NCH; hm <<= 1)
+#pragma unroll
+                for (int b = 0; b < NCH; ++b)
+                    if (!(b & hm))
+#pragma unroll
+                        for (int j = 0; j < 8; j += 2)
+                            butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * (b + hm) + j], v[8 * (b + hm) + j + 1]);
+            float amax = 0.0f;
+            const float2 c2 = make_float2(p.rot_c, p.rot_c);
+#pragma unroll
+            for (int e = 0; e < DR; e += 2) {
+                const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
+                v[e] = t.x;
+                v[e + 1] = t.y;
+                amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
+            }
+            amax = block_amax(amax);
+            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            const float y = __frcp_rn(scale);
+            const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
+            if (live) {
+                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR;
+#pragma unroll
+                for (int b = 0; b < NCH; ++b) {
+                    uint32_t out[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float* u = v + 8 * b + 4 * e;
+                        const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
+                        const float2 bq = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
+                        out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(bq.x, bq.y) << 16);
+                    }
+                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * (b ^ z)), make_uint2(out[0], out[1]));
+                }
+            }
+          } else {
             constexpr int E = DR / TPR;               // elements per thread
             constexpr int NCH = E / 8;                // 16-byte chunks per thread
             const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
             const bool live = r < block_rows(blk);
-            // v[8 m + j] holds element 8 (TPR m + q) + j of row r
+            // v[8 m + j] holds element 8 (TPR (m ^ zr) + q) + j of row r: odd rows take their
+            // chunk groups in swapped pairs, so the two rows of a quarter-warp read different
+            // 64-byte halves of their lines instead of the same banks
+            const int zr = r & 1;
             float v[E];
 #pragma unroll
             for (int m = 0; m < NCH; ++m) {
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
                 if (live)
-                    w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * m + q)) * 2);
+                    w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * (m ^ zr) + q)) * 2);
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -272,9 +374,27 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     v[e + 1] = t.y;
                 }
             }
-            // h = 8 TPR, 16 TPR, ...: across chunks of a thread
+            // h = 8 TPR: chunk-group bit 0, swapped in odd rows: there the pair's registers
+            // hold (b, a), and x' = fma(x, -1, y) = a - b, y' = fma(y, 1, x) = a + b land in
+            // the right groups, each rounded once as in the sweep
+            {
+                const float sg = zr ? -1.0f : 1.0f;
+                const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
 #pragma unroll
-            for (int hm = 1; hm < NCH; hm <<= 1)
+                for (int m = 0; m < NCH; m += 2)
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        const float2 x = make_float2(v[8 * m + j], v[8 * m + j + 1]);
+                        const float2 y = make_float2(v[8 * (m + 1) + j], v[8 * (m + 1) + j + 1]);
+                        const float2 xn = __ffma2_rn(x, sg2, y);
+                        const float2 yn = __ffma2_rn(y, nsg2, x);
+                        v[8 * m + j] = xn.x; v[8 * m + j + 1] = xn.y;
+                        v[8 * (m + 1) + j] = yn.x; v[8 * (m + 1) + j + 1] = yn.y;
+                    }
+            }
+            // h = 16 TPR, 32 TPR, ...: the other chunk-group bits, not swapped
+#pragma unroll
+            for (int hm = 2; hm < NCH; hm <<= 1)
 #pragma unroll
                 for (int m = 0; m < NCH; ++m)
                     if (!(m & hm))
@@ -306,9 +426,10 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                         const float2 b = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
                         out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(b.x, b.y) << 16);
                     }
-                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * TPR * m), make_uint2(out[0], out[1]));
+                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * TPR * (m ^ zr)), make_uint2(out[0], out[1]));
                 }
             }
+          }
         }
         if (threadIdx.x == 0) p.scales[blk] = scale;
         // every thread is done with this stage (and with warp_max) before it is refilled
