@@ -100,13 +100,14 @@ __device__ __forceinline__ void butterfly2(float& a0, float& a1, float& b0, floa
     b0 = dif.x; b1 = dif.y;
 }
 
-// Launch shape per variant: plain, 512 threads; rotated d = 64, one thread per row of a
-// 128-row block (all butterflies in registers, no shuffles); rotated d = 128 and 256, four
-// threads per row (one thread per row measured 12 % slower at d = 128, where 254 registers
-// a thread leave two 4-warp CTAs per SM; 24 % faster at d = 64).  Rotated d <= 128: two
-// or more CTAs per SM.
+// Launch shape per variant: plain, 512 threads; rotated, a 128-row block with one thread
+// per row at d = 64 (all butterflies in registers, no shuffles), two at d = 128 (one
+// shuffle stage) and four at d = 256.  Measured per B16 H16 N8192 tensor: one thread per
+// row was 24 % faster than four at d = 64 but 12 % slower at d = 128 (254 registers a
+// thread leave two 4-warp CTAs per SM); two were 2 % faster than four at d = 128.
+// Rotated d <= 128: two or more CTAs per SM.
 template <int DR> struct QuantShape {
-    static constexpr int TPR = (DR == 64) ? 1 : 4;
+    static constexpr int TPR = (DR == 64) ? 1 : (DR == 128 ? 2 : 4);
     static constexpr int kThreads = (DR == 0) ? 512 : kQuantRows * TPR;
     static constexpr int kMinBlocks = (DR > 0 && DR <= 128) ? 2 : 1;
 };
@@ -327,10 +328,11 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
             constexpr int NCH = E / 8;                // 16-byte chunks per thread
             const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
             const bool live = r < block_rows(blk);
-            // v[8 m + j] holds element 8 (TPR (m ^ zr) + q) + j of row r: odd rows take their
-            // chunk groups in swapped pairs, so the two rows of a quarter-warp read different
-            // 64-byte halves of their lines instead of the same banks
-            const int zr = r & 1;
+            // v[8 m + j] holds element 8 (TPR (m ^ zr) + q) + j of row r: the 8 / TPR rows of a
+            // quarter-warp take their chunk groups in orders XORed by zr = r mod (8 / TPR), so
+            // they read different slots of their lines instead of the same banks
+            constexpr int ZB = (TPR == 4) ? 1 : 2;    // group bits swapped per row
+            const int zr = r & ((1 << ZB) - 1);
             float v[E];
 #pragma unroll
             for (int m = 0; m < NCH; ++m) {
@@ -374,27 +376,31 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     v[e + 1] = t.y;
                 }
             }
-            // h = 8 TPR: chunk-group bit 0, swapped in odd rows: there the pair's registers
-            // hold (b, a), and x' = fma(x, -1, y) = a - b, y' = fma(y, 1, x) = a + b land in
-            // the right groups, each rounded once as in the sweep
-            {
-                const float sg = zr ? -1.0f : 1.0f;
+            // h = 8 TPR, ...: chunk-group bits below ZB, swapped in rows with that bit of zr
+            // set: there the pair's registers hold (b, a), and x' = fma(x, -1, y) = a - b,
+            // y' = fma(y, 1, x) = a + b land in the right groups, each rounded once as in the sweep
+#pragma unroll
+            for (int k = 0; k < ZB; ++k) {
+                const int hm = 1 << k;
+                const float sg = ((zr >> k) & 1) ? -1.0f : 1.0f;
                 const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
 #pragma unroll
-                for (int m = 0; m < NCH; m += 2)
+                for (int m = 0; m < NCH; ++m) {
+                    if (m & hm) continue;
 #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
                         const float2 x = make_float2(v[8 * m + j], v[8 * m + j + 1]);
-                        const float2 y = make_float2(v[8 * (m + 1) + j], v[8 * (m + 1) + j + 1]);
+                        const float2 y = make_float2(v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
                         const float2 xn = __ffma2_rn(x, sg2, y);
                         const float2 yn = __ffma2_rn(y, nsg2, x);
                         v[8 * m + j] = xn.x; v[8 * m + j + 1] = xn.y;
-                        v[8 * (m + 1) + j] = yn.x; v[8 * (m + 1) + j + 1] = yn.y;
+                        v[8 * (m + hm) + j] = yn.x; v[8 * (m + hm) + j + 1] = yn.y;
                     }
+                }
             }
-            // h = 16 TPR, 32 TPR, ...: the other chunk-group bits, not swapped
+            // the other chunk-group bits, not swapped
 #pragma unroll
-            for (int hm = 2; hm < NCH; hm <<= 1)
+            for (int hm = 1 << ZB; hm < NCH; hm <<= 1)
 #pragma unroll
                 for (int m = 0; m < NCH; ++m)
                     if (!(m & hm))
