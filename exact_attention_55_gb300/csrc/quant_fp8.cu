@@ -227,215 +227,215 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
         } else {
             static_assert(DR == 64 || DR == 128 || DR == 256, "rotated head dim");
             constexpr int TPR = QuantShape<DR>::TPR;  // threads per row
-          if constexpr (TPR == 1) {
-            // One thread per row.  Register block b (8 elements) holds the row's 16-byte
-            // chunk b ^ z, z = r & 7: the eight rows of a quarter-warp then read eight
-            // different 16-byte slots of their 128-byte lines (rows 2 * DR bytes apart would
-            // otherwise hit the same banks).  The butterflies over chunk bits 0-2 (h = 8, 16,
-            // 32) pair register blocks b and b ^ 2^k whose chunks are swapped where bit k of
-            // z is set; there x' = fma(x, -1, y) = a - b and y' = fma(y, 1, x) = a + b land
-            // in the right chunks, each rounded once as in the sweep (sign sg = -1 for a
-            // swapped pair, +1 otherwise: x' = fma(x, sg, y), y' = fma(y, -sg, x)).
-            constexpr int NCH = DR / 8;               // chunks per row
-            const int r = threadIdx.x, z = r & 7;
-            const bool live = r < block_rows(blk);
-            float v[DR];
-#pragma unroll
-            for (int b = 0; b < NCH; ++b) {
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (b ^ z)) * 2);
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[8 * b + 2 * e] = bf16_lo(ww[e]);
-                    v[8 * b + 2 * e + 1] = bf16_hi(ww[e]);
-                }
-            }
-            // h = 1: neighbours inside a pair of registers
-#pragma unroll
-            for (int e = 0; e < DR; e += 2) {
-                const float a = v[e], bb = v[e + 1];
-                v[e] = __fadd_rn(a, bb);
-                v[e + 1] = __fsub_rn(a, bb);
-            }
-            // h = 2, 4: inside each chunk
-#pragma unroll
-            for (int h = 2; h < 8; h <<= 1)
-#pragma unroll
-                for (int b = 0; b < NCH; ++b)
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2)
-                        if (!(j & h)) butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * b + j + h], v[8 * b + j + h + 1]);
-            // h = 8, 16, 32: chunk bits 0-2, swapped per row by z
-#pragma unroll
-            for (int k = 0; k < 3; ++k) {
-                const float sg = ((z >> k) & 1) ? -1.0f : 1.0f;
-                const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
-#pragma unroll
+            if constexpr (TPR == 1) {
+                // One thread per row.  Register block b (8 elements) holds the row's 16-byte
+                // chunk b ^ z, z = r & 7: the eight rows of a quarter-warp then read eight
+                // different 16-byte slots of their 128-byte lines (rows 2 * DR bytes apart would
+                // otherwise hit the same banks).  The butterflies over chunk bits 0-2 (h = 8, 16,
+                // 32) pair register blocks b and b ^ 2^k whose chunks are swapped where bit k of
+                // z is set; there x' = fma(x, -1, y) = a - b and y' = fma(y, 1, x) = a + b land
+                // in the right chunks, each rounded once as in the sweep (sign sg = -1 for a
+                // swapped pair, +1 otherwise: x' = fma(x, sg, y), y' = fma(y, -sg, x)).
+                constexpr int NCH = DR / 8;               // chunks per row
+                const int r = threadIdx.x, z = r & 7;
+                const bool live = r < block_rows(blk);
+                float v[DR];
+    #pragma unroll
                 for (int b = 0; b < NCH; ++b) {
-                    if (b & (1 << k)) continue;
-                    const int b2 = b | (1 << k);
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const float2 x = make_float2(v[8 * b + j], v[8 * b + j + 1]);
-                        const float2 y = make_float2(v[8 * b2 + j], v[8 * b2 + j + 1]);
-                        const float2 xn = __ffma2_rn(x, sg2, y);
-                        const float2 yn = __ffma2_rn(y, nsg2, x);
-                        v[8 * b + j] = xn.x; v[8 * b + j + 1] = xn.y;
-                        v[8 * b2 + j] = yn.x; v[8 * b2 + j + 1] = yn.y;
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (b ^ z)) * 2);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * b + 2 * e] = bf16_lo(ww[e]);
+                        v[8 * b + 2 * e + 1] = bf16_hi(ww[e]);
                     }
                 }
-            }
-            // h = 64 (d = 128): chunk bit 3, not swapped
-#pragma unroll
-            for (int hm = 8; hm < NCH; hm <<= 1)
-#pragma unroll
-                for (int b = 0; b < NCH; ++b)
-                    if (!(b & hm))
-#pragma unroll
+                // h = 1: neighbours inside a pair of registers
+    #pragma unroll
+                for (int e = 0; e < DR; e += 2) {
+                    const float a = v[e], bb = v[e + 1];
+                    v[e] = __fadd_rn(a, bb);
+                    v[e + 1] = __fsub_rn(a, bb);
+                }
+                // h = 2, 4: inside each chunk
+    #pragma unroll
+                for (int h = 2; h < 8; h <<= 1)
+    #pragma unroll
+                    for (int b = 0; b < NCH; ++b)
+    #pragma unroll
                         for (int j = 0; j < 8; j += 2)
-                            butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * (b + hm) + j], v[8 * (b + hm) + j + 1]);
-            float amax = 0.0f;
-            const float2 c2 = make_float2(p.rot_c, p.rot_c);
-#pragma unroll
-            for (int e = 0; e < DR; e += 2) {
-                const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
-                v[e] = t.x;
-                v[e + 1] = t.y;
-                amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
-            }
-            amax = block_amax(amax);
-            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            const float y = __frcp_rn(scale);
-            const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
-            if (live) {
-                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR;
-#pragma unroll
-                for (int b = 0; b < NCH; ++b) {
-                    uint32_t out[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float* u = v + 8 * b + 4 * e;
-                        const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
-                        const float2 bq = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
-                        out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(bq.x, bq.y) << 16);
+                            if (!(j & h)) butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * b + j + h], v[8 * b + j + h + 1]);
+                // h = 8, 16, 32: chunk bits 0-2, swapped per row by z
+    #pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const float sg = ((z >> k) & 1) ? -1.0f : 1.0f;
+                    const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
+    #pragma unroll
+                    for (int b = 0; b < NCH; ++b) {
+                        if (b & (1 << k)) continue;
+                        const int b2 = b | (1 << k);
+    #pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            const float2 x = make_float2(v[8 * b + j], v[8 * b + j + 1]);
+                            const float2 y = make_float2(v[8 * b2 + j], v[8 * b2 + j + 1]);
+                            const float2 xn = __ffma2_rn(x, sg2, y);
+                            const float2 yn = __ffma2_rn(y, nsg2, x);
+                            v[8 * b + j] = xn.x; v[8 * b + j + 1] = xn.y;
+                            v[8 * b2 + j] = yn.x; v[8 * b2 + j + 1] = yn.y;
+                        }
                     }
-                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * (b ^ z)), make_uint2(out[0], out[1]));
                 }
-            }
-          } else {
-            constexpr int E = DR / TPR;               // elements per thread
-            constexpr int NCH = E / 8;                // 16-byte chunks per thread
-            const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
-            const bool live = r < block_rows(blk);
-            // v[8 m + j] holds element 8 (TPR (m ^ zr) + q) + j of row r: the 8 / TPR rows of a
-            // quarter-warp take their chunk groups in orders XORed by zr = r mod (8 / TPR), so
-            // they read different slots of their lines instead of the same banks
-            constexpr int ZB = (TPR == 4) ? 1 : 2;    // group bits swapped per row
-            const int zr = r & ((1 << ZB) - 1);
-            float v[E];
-#pragma unroll
-            for (int m = 0; m < NCH; ++m) {
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (live)
-                    w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * (m ^ zr) + q)) * 2);
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[8 * m + 2 * e] = bf16_lo(ww[e]);
-                    v[8 * m + 2 * e + 1] = bf16_hi(ww[e]);
-                }
-            }
-            // h = 1: neighbours inside a pair of registers
-#pragma unroll
-            for (int e = 0; e < E; e += 2) {
-                const float a = v[e], b = v[e + 1];
-                v[e] = __fadd_rn(a, b);
-                v[e + 1] = __fsub_rn(a, b);
-            }
-            // h = 2, 4: inside each chunk, two butterflies per packed instruction
-#pragma unroll
-            for (int h = 2; h < 8; h <<= 1)
-#pragma unroll
-                for (int m = 0; m < NCH; ++m)
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2)
-                        if (!(j & h)) butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * m + j + h], v[8 * m + j + h + 1]);
-            // h = 8, 16, ..., 4 TPR: across the row's lanes; the lower lane keeps v + o
-            // and the upper one o - v, both as fma(v, +-1, o)
-#pragma unroll
-            for (int lb = 0; (1 << lb) < TPR; ++lb) {
-                const float sg = ((q >> lb) & 1) ? -1.0f : 1.0f;
-                const float2 sg2 = make_float2(sg, sg);
-#pragma unroll
-                for (int e = 0; e < E; e += 2) {
-                    const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], 1 << lb),
-                                                 __shfl_xor_sync(0xffffffffu, v[e + 1], 1 << lb));
-                    const float2 t = __ffma2_rn(make_float2(v[e], v[e + 1]), sg2, o);
+                // chunk bits from 3 up (none at d = 64), not swapped
+    #pragma unroll
+                for (int hm = 8; hm < NCH; hm <<= 1)
+    #pragma unroll
+                    for (int b = 0; b < NCH; ++b)
+                        if (!(b & hm))
+    #pragma unroll
+                            for (int j = 0; j < 8; j += 2)
+                                butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * (b + hm) + j], v[8 * (b + hm) + j + 1]);
+                float amax = 0.0f;
+                const float2 c2 = make_float2(p.rot_c, p.rot_c);
+    #pragma unroll
+                for (int e = 0; e < DR; e += 2) {
+                    const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
                     v[e] = t.x;
                     v[e + 1] = t.y;
+                    amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
                 }
-            }
-            // h = 8 TPR, ...: chunk-group bits below ZB, swapped in rows with that bit of zr
-            // set: there the pair's registers hold (b, a), and x' = fma(x, -1, y) = a - b,
-            // y' = fma(y, 1, x) = a + b land in the right groups, each rounded once as in the sweep
-#pragma unroll
-            for (int k = 0; k < ZB; ++k) {
-                const int hm = 1 << k;
-                const float sg = ((zr >> k) & 1) ? -1.0f : 1.0f;
-                const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
-#pragma unroll
-                for (int m = 0; m < NCH; ++m) {
-                    if (m & hm) continue;
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const float2 x = make_float2(v[8 * m + j], v[8 * m + j + 1]);
-                        const float2 y = make_float2(v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
-                        const float2 xn = __ffma2_rn(x, sg2, y);
-                        const float2 yn = __ffma2_rn(y, nsg2, x);
-                        v[8 * m + j] = xn.x; v[8 * m + j + 1] = xn.y;
-                        v[8 * (m + hm) + j] = yn.x; v[8 * (m + hm) + j + 1] = yn.y;
+                amax = block_amax(amax);
+                scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                const float y = __frcp_rn(scale);
+                const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
+                if (live) {
+                    uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR;
+    #pragma unroll
+                    for (int b = 0; b < NCH; ++b) {
+                        uint32_t out[2];
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float* u = v + 8 * b + 4 * e;
+                            const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
+                            const float2 bq = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
+                            out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(bq.x, bq.y) << 16);
+                        }
+                        __stcs(reinterpret_cast<uint2*>(row8 + 8 * (b ^ z)), make_uint2(out[0], out[1]));
                     }
                 }
-            }
-            // the other chunk-group bits, not swapped
-#pragma unroll
-            for (int hm = 1 << ZB; hm < NCH; hm <<= 1)
-#pragma unroll
-                for (int m = 0; m < NCH; ++m)
-                    if (!(m & hm))
-#pragma unroll
+            } else {
+                constexpr int E = DR / TPR;               // elements per thread
+                constexpr int NCH = E / 8;                // 16-byte chunks per thread
+                const int r = threadIdx.x / TPR, q = threadIdx.x % TPR;
+                const bool live = r < block_rows(blk);
+                // v[8 m + j] holds element 8 (TPR (m ^ zr) + q) + j of row r: the 8 / TPR rows of a
+                // quarter-warp take their chunk groups in orders XORed by zr = r mod (8 / TPR), so
+                // they read different slots of their lines instead of the same banks
+                constexpr int ZB = (TPR == 4) ? 1 : 2;    // group bits swapped per row
+                const int zr = r & ((1 << ZB) - 1);
+                float v[E];
+    #pragma unroll
+                for (int m = 0; m < NCH; ++m) {
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (live)
+                        w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * (m ^ zr) + q)) * 2);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        v[8 * m + 2 * e] = bf16_lo(ww[e]);
+                        v[8 * m + 2 * e + 1] = bf16_hi(ww[e]);
+                    }
+                }
+                // h = 1: neighbours inside a pair of registers
+    #pragma unroll
+                for (int e = 0; e < E; e += 2) {
+                    const float a = v[e], b = v[e + 1];
+                    v[e] = __fadd_rn(a, b);
+                    v[e + 1] = __fsub_rn(a, b);
+                }
+                // h = 2, 4: inside each chunk, two butterflies per packed instruction
+    #pragma unroll
+                for (int h = 2; h < 8; h <<= 1)
+    #pragma unroll
+                    for (int m = 0; m < NCH; ++m)
+    #pragma unroll
                         for (int j = 0; j < 8; j += 2)
-                            butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
-            float amax = 0.0f;
-            const float2 c2 = make_float2(p.rot_c, p.rot_c);
-#pragma unroll
-            for (int e = 0; e < E; e += 2) {
-                const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
-                v[e] = t.x;
-                v[e + 1] = t.y;
-                amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
-            }
-            amax = block_amax(amax);
-            scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            const float y = __frcp_rn(scale);
-            const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
-            if (live) {
-                uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;  // chunk TPR m + q
-#pragma unroll
-                for (int m = 0; m < NCH; ++m) {
-                    uint32_t out[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float* u = v + 8 * m + 4 * e;
-                        const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
-                        const float2 b = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
-                        out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(b.x, b.y) << 16);
+                            if (!(j & h)) butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * m + j + h], v[8 * m + j + h + 1]);
+                // h = 8, 16, ..., 4 TPR: across the row's lanes; the lower lane keeps v + o
+                // and the upper one o - v, both as fma(v, +-1, o)
+    #pragma unroll
+                for (int lb = 0; (1 << lb) < TPR; ++lb) {
+                    const float sg = ((q >> lb) & 1) ? -1.0f : 1.0f;
+                    const float2 sg2 = make_float2(sg, sg);
+    #pragma unroll
+                    for (int e = 0; e < E; e += 2) {
+                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], 1 << lb),
+                                                     __shfl_xor_sync(0xffffffffu, v[e + 1], 1 << lb));
+                        const float2 t = __ffma2_rn(make_float2(v[e], v[e + 1]), sg2, o);
+                        v[e] = t.x;
+                        v[e + 1] = t.y;
                     }
-                    __stcs(reinterpret_cast<uint2*>(row8 + 8 * TPR * (m ^ zr)), make_uint2(out[0], out[1]));
+                }
+                // h = 8 TPR, ...: chunk-group bits below ZB, swapped in rows with that bit of zr
+                // set: there the pair's registers hold (b, a), and x' = fma(x, -1, y) = a - b,
+                // y' = fma(y, 1, x) = a + b land in the right groups, each rounded once as in the sweep
+    #pragma unroll
+                for (int k = 0; k < ZB; ++k) {
+                    const int hm = 1 << k;
+                    const float sg = ((zr >> k) & 1) ? -1.0f : 1.0f;
+                    const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
+    #pragma unroll
+                    for (int m = 0; m < NCH; ++m) {
+                        if (m & hm) continue;
+    #pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            const float2 x = make_float2(v[8 * m + j], v[8 * m + j + 1]);
+                            const float2 y = make_float2(v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
+                            const float2 xn = __ffma2_rn(x, sg2, y);
+                            const float2 yn = __ffma2_rn(y, nsg2, x);
+                            v[8 * m + j] = xn.x; v[8 * m + j + 1] = xn.y;
+                            v[8 * (m + hm) + j] = yn.x; v[8 * (m + hm) + j + 1] = yn.y;
+                        }
+                    }
+                }
+                // the other chunk-group bits, not swapped
+    #pragma unroll
+                for (int hm = 1 << ZB; hm < NCH; hm <<= 1)
+    #pragma unroll
+                    for (int m = 0; m < NCH; ++m)
+                        if (!(m & hm))
+    #pragma unroll
+                            for (int j = 0; j < 8; j += 2)
+                                butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
+                float amax = 0.0f;
+                const float2 c2 = make_float2(p.rot_c, p.rot_c);
+    #pragma unroll
+                for (int e = 0; e < E; e += 2) {
+                    const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
+                    v[e] = t.x;
+                    v[e + 1] = t.y;
+                    amax = fmax3(amax, fabsf(t.x), fabsf(t.y));
+                }
+                amax = block_amax(amax);
+                scale = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                const float y = __frcp_rn(scale);
+                const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
+                if (live) {
+                    uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;  // chunk TPR m + q
+    #pragma unroll
+                    for (int m = 0; m < NCH; ++m) {
+                        uint32_t out[2];
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float* u = v + 8 * m + 4 * e;
+                            const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
+                            const float2 b = div2_by_scale(make_float2(u[2], u[3]), sn2, y2);
+                            out[e] = (uint32_t)pack_e4m3x2(a.x, a.y) | ((uint32_t)pack_e4m3x2(b.x, b.y) << 16);
+                        }
+                        __stcs(reinterpret_cast<uint2*>(row8 + 8 * TPR * (m ^ zr)), make_uint2(out[0], out[1]));
+                    }
                 }
             }
-          }
         }
         if (threadIdx.x == 0) p.scales[blk] = scale;
         // every thread is done with this stage (and with warp_max) before it is refilled
