@@ -240,42 +240,42 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 const int r = threadIdx.x, z = r & 7;
                 const bool live = r < block_rows(blk);
                 float v[DR];
-    #pragma unroll
+#pragma unroll
                 for (int b = 0; b < NCH; ++b) {
                     uint4 w = make_uint4(0u, 0u, 0u, 0u);
                     if (live) w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (b ^ z)) * 2);
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         v[8 * b + 2 * e] = bf16_lo(ww[e]);
                         v[8 * b + 2 * e + 1] = bf16_hi(ww[e]);
                     }
                 }
                 // h = 1: neighbours inside a pair of registers
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < DR; e += 2) {
                     const float a = v[e], bb = v[e + 1];
                     v[e] = __fadd_rn(a, bb);
                     v[e + 1] = __fsub_rn(a, bb);
                 }
                 // h = 2, 4: inside each chunk
-    #pragma unroll
+#pragma unroll
                 for (int h = 2; h < 8; h <<= 1)
-    #pragma unroll
+#pragma unroll
                     for (int b = 0; b < NCH; ++b)
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 8; j += 2)
                             if (!(j & h)) butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * b + j + h], v[8 * b + j + h + 1]);
                 // h = 8, 16, 32: chunk bits 0-2, swapped per row by z
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < 3; ++k) {
                     const float sg = ((z >> k) & 1) ? -1.0f : 1.0f;
                     const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
-    #pragma unroll
+#pragma unroll
                     for (int b = 0; b < NCH; ++b) {
                         if (b & (1 << k)) continue;
                         const int b2 = b | (1 << k);
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 8; j += 2) {
                             const float2 x = make_float2(v[8 * b + j], v[8 * b + j + 1]);
                             const float2 y = make_float2(v[8 * b2 + j], v[8 * b2 + j + 1]);
@@ -287,17 +287,17 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     }
                 }
                 // chunk bits from 3 up (none at d = 64), not swapped
-    #pragma unroll
+#pragma unroll
                 for (int hm = 8; hm < NCH; hm <<= 1)
-    #pragma unroll
+#pragma unroll
                     for (int b = 0; b < NCH; ++b)
                         if (!(b & hm))
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 8; j += 2)
                                 butterfly2(v[8 * b + j], v[8 * b + j + 1], v[8 * (b + hm) + j], v[8 * (b + hm) + j + 1]);
                 float amax = 0.0f;
                 const float2 c2 = make_float2(p.rot_c, p.rot_c);
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < DR; e += 2) {
                     const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
                     v[e] = t.x;
@@ -310,10 +310,10 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
                 if (live) {
                     uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR;
-    #pragma unroll
+#pragma unroll
                     for (int b = 0; b < NCH; ++b) {
                         uint32_t out[2];
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const float* u = v + 8 * b + 4 * e;
                             const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
@@ -334,40 +334,40 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 constexpr int ZB = (TPR == 4) ? 1 : 2;    // group bits swapped per row
                 const int zr = r & ((1 << ZB) - 1);
                 float v[E];
-    #pragma unroll
+#pragma unroll
                 for (int m = 0; m < NCH; ++m) {
                     uint4 w = make_uint4(0u, 0u, 0u, 0u);
                     if (live)
                         w = *reinterpret_cast<const uint4*>(st + ((size_t)r * DR + 8 * (TPR * (m ^ zr) + q)) * 2);
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         v[8 * m + 2 * e] = bf16_lo(ww[e]);
                         v[8 * m + 2 * e + 1] = bf16_hi(ww[e]);
                     }
                 }
                 // h = 1: neighbours inside a pair of registers
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < E; e += 2) {
                     const float a = v[e], b = v[e + 1];
                     v[e] = __fadd_rn(a, b);
                     v[e + 1] = __fsub_rn(a, b);
                 }
                 // h = 2, 4: inside each chunk, two butterflies per packed instruction
-    #pragma unroll
+#pragma unroll
                 for (int h = 2; h < 8; h <<= 1)
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < NCH; ++m)
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 8; j += 2)
                             if (!(j & h)) butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * m + j + h], v[8 * m + j + h + 1]);
                 // h = 8, 16, ..., 4 TPR: across the row's lanes; the lower lane keeps v + o
                 // and the upper one o - v, both as fma(v, +-1, o)
-    #pragma unroll
+#pragma unroll
                 for (int lb = 0; (1 << lb) < TPR; ++lb) {
                     const float sg = ((q >> lb) & 1) ? -1.0f : 1.0f;
                     const float2 sg2 = make_float2(sg, sg);
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < E; e += 2) {
                         const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[e], 1 << lb),
                                                      __shfl_xor_sync(0xffffffffu, v[e + 1], 1 << lb));
@@ -379,15 +379,15 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 // h = 8 TPR, ...: chunk-group bits below ZB, swapped in rows with that bit of zr
                 // set: there the pair's registers hold (b, a), and x' = fma(x, -1, y) = a - b,
                 // y' = fma(y, 1, x) = a + b land in the right groups, each rounded once as in the sweep
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < ZB; ++k) {
                     const int hm = 1 << k;
                     const float sg = ((zr >> k) & 1) ? -1.0f : 1.0f;
                     const float2 sg2 = make_float2(sg, sg), nsg2 = make_float2(-sg, -sg);
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < NCH; ++m) {
                         if (m & hm) continue;
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 8; j += 2) {
                             const float2 x = make_float2(v[8 * m + j], v[8 * m + j + 1]);
                             const float2 y = make_float2(v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
@@ -399,17 +399,17 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                     }
                 }
                 // the other chunk-group bits, not swapped
-    #pragma unroll
+#pragma unroll
                 for (int hm = 1 << ZB; hm < NCH; hm <<= 1)
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < NCH; ++m)
                         if (!(m & hm))
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 8; j += 2)
                                 butterfly2(v[8 * m + j], v[8 * m + j + 1], v[8 * (m + hm) + j], v[8 * (m + hm) + j + 1]);
                 float amax = 0.0f;
                 const float2 c2 = make_float2(p.rot_c, p.rot_c);
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < E; e += 2) {
                     const float2 t = __fmul2_rn(make_float2(v[e], v[e + 1]), c2);
                     v[e] = t.x;
@@ -422,10 +422,10 @@ __global__ void __launch_bounds__(QuantShape<DR>::kThreads, QuantShape<DR>::kMin
                 const float2 y2 = make_float2(y, y), sn2 = make_float2(-scale, -scale);
                 if (live) {
                     uint8_t* row8 = p.x8 + block_base(blk) + (size_t)r * DR + 8 * q;  // chunk TPR m + q
-    #pragma unroll
+#pragma unroll
                     for (int m = 0; m < NCH; ++m) {
                         uint32_t out[2];
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const float* u = v + 8 * m + 4 * e;
                             const float2 a = div2_by_scale(make_float2(u[0], u[1]), sn2, y2);
