@@ -32,7 +32,7 @@ __all__ = [
     "attn_decode_workspace_bytes",
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_hadamard", "attn_fwd_fp8",
     "attn_quantize_fp8_blockwise_fmt", "attn_fwd_fp8_fmt", "attn_fwd_fp8_blocks",
-    "attn_fp8_qk_block_rows", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
+    "attn_fp8_qk_block_rows", "attn_fwd_schedule", "ATTN_FP8_E4M3", "ATTN_FP8_E5M2",
     "ATTN_FP8_E4M3_POW2",
     "attn_status_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "attn_selftest_fwd_withheld_load", "attn_selftest_quant_withheld_load",
@@ -61,7 +61,7 @@ EXPORTED_SYMBOLS = (
     "attn_quantize_fp8_blockwise", "attn_quantize_fp8_blockwise_fmt",
     "attn_quantize_fp8_hadamard",
     "attn_fwd_fp8", "attn_fwd_fp8_fmt", "attn_fwd_fp8_blocks", "attn_fp8_qk_block_rows",
-    "attn_status_string", "attn_get_device_status",
+    "attn_fwd_schedule", "attn_status_string", "attn_get_device_status",
     "attn_selftest_wait_timeout", "attn_selftest_fwd_withheld_load",
     "attn_selftest_quant_withheld_load", "attn_selftest_bwd_withheld_load",
     "attn_selftest_fp8_convert",
@@ -128,6 +128,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_fp8_blocks.restype = i
         lib.attn_fp8_qk_block_rows.argtypes = [i]
         lib.attn_fp8_qk_block_rows.restype = i
+        lib.attn_fwd_schedule.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+        lib.attn_fwd_schedule.restype = i
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_get_device_status.argtypes = [vp]
@@ -479,6 +481,19 @@ def attn_fwd_fp8_blocks(q8, k8, v8, descale_q, descale_k, descale_v, qk_block: i
 def attn_fp8_qk_block_rows(d: int) -> int:
     """Rows per Q / K scale block under head-dim-aware scaling: min(d, 128)."""
     return int(load_library().attn_fp8_qk_block_rows(int(d)))
+
+
+def attn_fwd_schedule(B: int, H: int, N: int, d: int, causal: bool = False, window: int = 0,
+                      sm_count: int = 152) -> dict:
+    """How a batched forward call would spread its work over sm_count SMs (no device is
+    touched): the walk (0 pairs, 1 single units with a plain stride, 2 rotated), the grid,
+    the number of sub-units, the walk's constants and the query blocks per head."""
+    out = (ctypes.c_int * 8)()
+    st = load_library().attn_fwd_schedule(int(B), int(H), int(N), int(d), int(bool(causal)),
+                                          int(window), int(sm_count), out)
+    _raise_if(st, "attn_fwd_schedule")
+    keys = ("walk", "grid", "subs", "first", "a", "m", "step", "num_qblk")
+    return dict(zip(keys, (int(x) for x in out)))
 
 
 def _fwd_fp8(entry, qk_fmt, q8, k8, v8, descale_q, descale_k, descale_v, scale, causal, window,

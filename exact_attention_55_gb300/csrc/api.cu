@@ -442,6 +442,34 @@ extern "C" int attn_fp8_qk_block_rows(int d)
     return d < 128 ? d : 128;
 }
 
+extern "C" attn_status_t attn_fwd_schedule(int B, int H, int N, int d, int causal, int window,
+                                           int sm_count, int* out)
+{
+    if (out == nullptr || sm_count < 1) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+    const int unit_rows = d == 256 ? FwdCfg<256, false>::NQ * FwdCfg<256, false>::BM
+                                   : FwdCfg<128, false>::NQ * FwdCfg<128, false>::BM;
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.num_qblk = (N + unit_rows - 1) / unit_rows;
+    const long long pairs = (long long)B * H * ((p.num_qblk + 1) / 2);
+    if (2 * pairs + 4LL * sm_count > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    p.num_units = (int)pairs;
+    p.unit_walk = single_unit_walk(causal, window, N, pairs, sm_count);
+    const int grid = fwd_grid(p, sm_count);
+    set_fwd_walk(p, grid);
+    out[0] = p.unit_walk;
+    out[1] = grid;
+    out[2] = 2 * p.num_units;
+    out[3] = p.walk_first;
+    out[4] = p.walk_a;
+    out[5] = p.walk_m;
+    out[6] = p.walk_step;
+    out[7] = p.num_qblk;
+    return ATTN_OK;
+}
+
 static attn_status_t quantize(const void* x, void* x8, float* scales, int B, int H, int N, int d,
                               int block, bool rotate, void* stream, int fmt = ATTN_FP8_E4M3,
                               unsigned long long timeout_ns = kWaitTimeoutNs, int withhold = 0)

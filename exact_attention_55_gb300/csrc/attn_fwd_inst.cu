@@ -39,16 +39,9 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, cons
         if (e != cudaSuccess) return e;
         if (attr.numRegs * C::NUM_THREADS < C::REG_POOL) return cudaErrorInvalidConfiguration;
     }
-    const int subs = p.unit_walk ? 2 * p.num_units : p.num_units;  // what the CTAs stride over
-    const int grid = subs < sm_count ? subs : sm_count;
+    const int grid = fwd_grid(p, sm_count);
     FwdParams q = p;
-    if (p.unit_walk == 0) {          // pairs: 2c, 2c + 1, 2c + 2G, 2c + 2G + 1, ...
-        q.walk_first = 2, q.walk_a = 0, q.walk_m = 2, q.walk_step = 2 * grid - 2;
-    } else if (p.unit_walk == 1) {   // single units, plain stride: c, c + G, ...
-        q.walk_first = 1, q.walk_a = 1, q.walk_m = 0x7fffffff, q.walk_step = grid - 1;
-    } else {                         // single units, rotated rounds
-        q.walk_first = 1, q.walk_a = 1, q.walk_m = grid, q.walk_step = grid;
-    }
+    set_fwd_walk(q, grid);
     kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmO, q);
     return cudaGetLastError();
 }

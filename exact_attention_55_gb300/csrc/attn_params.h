@@ -57,6 +57,28 @@ struct FwdParams {
     int T;
 };
 
+// Grid of a forward launch on sm_count SMs (one CTA per SM): pairs, or single units under
+// the single-unit walks, whichever the CTAs stride over, at most one per SM.
+inline int fwd_grid(const FwdParams& p, int sm_count)
+{
+    const int items = p.unit_walk ? 2 * p.num_units : p.num_units;
+    return items < sm_count ? items : sm_count;
+}
+
+// The batched walk's constants for a launch of `grid` CTAs: CTA c starts at sub-unit
+// c * walk_first and after s goes to s + 1 when (s + walk_a) % walk_m == 0, else to
+// s + 1 + walk_step (the kernel's first_sub / next_sub).
+inline void set_fwd_walk(FwdParams& p, int grid)
+{
+    if (p.unit_walk == 0) {          // pairs: 2c, 2c + 1, 2c + 2G, 2c + 2G + 1, ...
+        p.walk_first = 2, p.walk_a = 0, p.walk_m = 2, p.walk_step = 2 * grid - 2;
+    } else if (p.unit_walk == 1) {   // single units, plain stride: c, c + G, ...
+        p.walk_first = 1, p.walk_a = 1, p.walk_m = 0x7fffffff, p.walk_step = grid - 1;
+    } else {                         // single units, rotated rounds
+        p.walk_first = 1, p.walk_a = 1, p.walk_m = grid, p.walk_step = grid;
+    }
+}
+
 // Backward pass (attn_bwd.cu).  Tensors [BH, N, D] bf16; lse / delta [BH, N] fp32.
 struct BwdParams {
     const void* o;        // forward output

@@ -299,6 +299,26 @@ attn_status_t attn_fwd_fp8_fmt(const void* q8, const void* k8, const void* v8,
                                int v_format, void* stream);
 
 /*
+ * attn_fwd_schedule -- how a batched forward call (attn_fwd_bf16, attn_fwd_fp8 and its
+ * variants) with these sizes and mask would spread its work over sm_count SMs: the
+ * persistent grid and its walk over the work units ([YT] §1.2 asks for the work to be
+ * balanced over the SMs).  A diagnostic: no device memory, stream or kernel is touched.
+ *
+ * A work unit is (head, query block of 256 rows; 128 at d = 256); sub-unit s is half
+ * s & 1 of the complementary pair s >> 1 of query blocks (nq-1-k, k) of a head.
+ *   out : int[8], written: [0] walk (0 whole pairs -- causal masks; 1 single units with a
+ *         plain stride -- no mask, when that takes fewer rounds; 2 single units in
+ *         rotated rounds -- windows), [1] grid (CTAs), [2] sub-units, [3..6] the walk's
+ *         constants first, a, m, step: CTA c starts at sub-unit c * first and after s goes
+ *         to s + 1 when (s + a) % m == 0, else to s + 1 + step, while s < out[2],
+ *         [7] query blocks per head
+ *   d in {64, 128, 256} (else ATTN_ERR_UNSUPPORTED); B, H, N, sm_count >= 1 and out
+ *   non-null (else ATTN_ERR_INVALID_ARG)
+ */
+attn_status_t attn_fwd_schedule(int B, int H, int N, int d, int causal, int window,
+                                int sm_count, int* out);
+
+/*
  * attn_fp8_qk_block_rows -- rows per Q and K scale block under head-dim-aware
  * scaling: min(d, 128) (0 for d < 1).
  *
